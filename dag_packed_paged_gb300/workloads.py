@@ -1,0 +1,417 @@
+"""Seeded synthetic episodes (DAG topology + bf16 tensors) for tests and benchmarks.
+
+This module is the one piece shared by the CUDA path's tests/benchmark and the
+CPU oracle's tests.  It holds no attention arithmetic: it only draws episode
+shapes (branches with parent / fork offset / length, mount edges, a page
+table) and random tensors, rounds them to bf16, and scatters K/V rows into a
+paged pool.  Nothing here computes visibility, positions or attention.
+
+Episode model (Octopus, arXiv 2611.06956, Section 3 and Section 3.3 item 1):
+an episode is a DAG of branches.  Tree edges are forks: a child branch starts
+after ``fork_offset`` rows of its parent.  Mount edges lend a completed span
+``[src_begin, src_end)`` of a source branch to a reader branch from the
+reader's row ``reader_offset`` onwards.  Every branch's rows are stored once,
+contiguously, in a compact row strip (``row_start`` .. ``row_start+length``),
+branches laid out in depth-first order (Section 3.3 item 2: nodes
+"concatenated topologically").
+
+Tensor recipe: fp32 draws from ``numpy.random.default_rng`` on a
+``SeedSequence`` stream separate from the topology streams, in the order
+Q [N,Hq,D], K [N,Hkv,D], V [N,Hkv,D], dO [N,Hq,D], scaled, then rounded to
+bf16 with round-to-nearest-even.  K and V are written into a page pool
+[n_pages, P, Hkv, D] through a seeded random page permutation with about 5%
+spare pages; spare pages hold NaN so that any stray read shows up, and rows of
+the last logical page beyond N hold zeros.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+BRANCH_DTYPE = np.dtype(
+    [("parent", "<i4"), ("fork_offset", "<i4"), ("length", "<i4"), ("row_start", "<i8")],
+    align=True)
+MOUNT_DTYPE = np.dtype(
+    [("reader", "<i4"), ("reader_offset", "<i4"), ("source", "<i4"),
+     ("src_begin", "<i4"), ("src_end", "<i4")], align=True)
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+@dataclasses.dataclass
+class Episode:
+    """One packed episode: topology plus the attention shape it is run with."""
+    name: str
+    branches: np.ndarray          # BRANCH_DTYPE[n_branches]
+    mounts: np.ndarray            # MOUNT_DTYPE[n_mounts]
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    seed: int = 0
+    info: dict = dataclasses.field(default_factory=dict)
+
+    @property
+    def n_rows(self) -> int:
+        b = self.branches
+        return int((b["row_start"] + b["length"]).max()) if len(b) else 0
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+@dataclasses.dataclass
+class Tensors:
+    """bf16 tensors (stored as uint16 bit patterns) in compact-row layout."""
+    q: np.ndarray    # [N, Hq, D]
+    k: np.ndarray    # [N, Hkv, D]
+    v: np.ndarray    # [N, Hkv, D]
+    do: np.ndarray   # [N, Hq, D]
+
+
+@dataclasses.dataclass
+class Pool:
+    """Paged K/V storage: logical page l of the strip lives in physical page page_table[l]."""
+    page_table: np.ndarray   # int32 [n_logical_pages]
+    k_pool: np.ndarray       # uint16 [n_pages, P, Hkv, D]
+    v_pool: np.ndarray       # uint16 [n_pages, P, Hkv, D]
+
+
+# --------------------------------------------------------------------------------------
+# bf16 helpers (storage format only)
+# --------------------------------------------------------------------------------------
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 to bf16 with round-to-nearest-even; returns uint16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# --------------------------------------------------------------------------------------
+# topology helpers
+# --------------------------------------------------------------------------------------
+
+def _layout_dfs(parents: list[int], lengths: list[int], order_key=None) -> np.ndarray:
+    """Assign row_start to branches in depth-first order (children by index)."""
+    n = len(parents)
+    children = [[] for _ in range(n)]
+    roots = []
+    for i, p in enumerate(parents):
+        (roots if p < 0 else children[p]).append(i)
+    row_start = [0] * n
+    cur = 0
+    stack = list(reversed(roots))
+    while stack:
+        u = stack.pop()
+        row_start[u] = cur
+        cur += lengths[u]
+        stack.extend(reversed(children[u]))
+    return np.array(row_start, dtype=np.int64)
+
+
+def make_branches(parents, fork_offsets, lengths) -> np.ndarray:
+    br = np.zeros(len(parents), dtype=BRANCH_DTYPE)
+    br["parent"] = parents
+    br["fork_offset"] = fork_offsets
+    br["length"] = lengths
+    br["row_start"] = _layout_dfs(list(parents), list(lengths))
+    return br
+
+
+def make_mounts(rows) -> np.ndarray:
+    m = np.zeros(len(rows), dtype=MOUNT_DTYPE)
+    for i, (r, t, s, b, e) in enumerate(rows):
+        m[i] = (r, t, s, b, e)
+    return m
+
+
+def _streams(seed: int, n: int):
+    return [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(n)]
+
+
+# --------------------------------------------------------------------------------------
+# the five workload shapes
+# --------------------------------------------------------------------------------------
+
+def tiny(seed: int = 0) -> Episode:
+    """Root of 256 rows; three 128-row branches forking at 256; branch 2 mounts
+    branch 1's rows [64,128) from its own row 64.  4 query / 1 KV head, D=64, page 16."""
+    br = make_branches([-1, 0, 0, 0], [0, 256, 256, 256], [256, 128, 128, 128])
+    mt = make_mounts([(2, 64, 1, 64, 128)])
+    return Episode("tiny_tree", br, mt, 4, 1, 64, 16, seed)
+
+
+def balanced(seed: int = 0) -> Episode:
+    """4096-row root, fan-out 4 at depth 1 and 2 (16 leaves), every edge 2048 rows, no mounts.
+    GQA 16/4, D=128, page 64."""
+    parents, forks, lens = [-1], [0], [4096]
+    for _ in range(4):
+        c = len(parents)
+        parents.append(0); forks.append(4096); lens.append(2048)
+        for _ in range(4):
+            parents.append(c); forks.append(2048); lens.append(2048)
+    return Episode("balanced_tree", make_branches(parents, forks, lens),
+                   make_mounts([]), 16, 4, 128, 64, seed)
+
+
+def _commander_dag(rng_len, rng_mount, root_len, n_workers, len_lo, len_hi, n_mounts,
+                   page=64, max_pages=4):
+    lens = [root_len] + [int(x) for x in rng_len.integers(len_lo, len_hi + 1, size=n_workers)]
+    parents = [-1] + [0] * n_workers
+    forks = [0] + [root_len] * n_workers
+    # completion order: a worker may only read workers that completed before it
+    order = rng_mount.permutation(np.arange(1, n_workers + 1))
+    rank = {int(w): i for i, w in enumerate(order)}
+    pairs = [(r, s) for r in range(1, n_workers + 1) for s in range(1, n_workers + 1)
+             if r != s and rank[s] < rank[r]]
+    pick = rng_mount.choice(len(pairs), size=n_mounts, replace=False)
+    mounts = []
+    for idx in sorted(int(i) for i in pick):
+        r, s = pairs[idx]
+        k = int(rng_mount.integers(1, max_pages + 1))
+        span = min(page * k, lens[s])
+        t = int(rng_mount.integers(1, lens[r]))       # uniform in [1, len-1]
+        mounts.append((r, t, s, lens[s] - span, lens[s]))
+    return parents, forks, lens, mounts
+
+
+def commander_worker(seed: int = 0) -> Episode:
+    """8192-row commander root forking 8 workers with lengths uniform in [8192, 32768];
+    12 mount edges, each lending 1-4 64-row pages from a sibling's tail at a uniform
+    point of the reader; sources complete before their readers.  GQA 16/4, D=128, page 64."""
+    rl, rm = _streams(seed, 2)
+    parents, forks, lens, mounts = _commander_dag(rl, rm, 8192, 8, 8192, 32768, 12)
+    return Episode("commander_worker_dag", make_branches(parents, forks, lens),
+                   make_mounts(mounts), 16, 4, 128, 64, seed)
+
+
+def _irregular_topology(seed: int, rho: float, n_edges: int = 64):
+    r_len, r_par, r_fork = _streams(seed, 3)
+    lens = np.clip(np.round(r_len.lognormal(7.0, 1.0, size=n_edges)), 16, 16384).astype(int)
+    u = r_par.random(size=n_edges)
+    pick = r_par.random(size=n_edges)
+    fork_u = r_fork.random(size=n_edges)
+    parents, forks = [-1], [0]
+    for k in range(1, n_edges):
+        p = k - 1 if u[k] < rho else int(pick[k] * k)          # newest edge, else uniform earlier
+        f = 1 + int(fork_u[k] * (lens[p] - 1))                  # uniform in [1, len_p - 1]
+        parents.append(p)
+        forks.append(f)
+    return parents, forks, [int(x) for x in lens]
+
+
+def _expanded_rows(parents, forks, lens):
+    """Sum of the lengths of the root-to-edge-end trajectories (one per edge)."""
+    pre = [0] * len(parents)
+    for k in range(len(parents)):
+        pre[k] = 0 if parents[k] < 0 else pre[parents[k]] + forks[k]
+    return sum(pre[k] + lens[k] for k in range(len(parents)))
+
+
+def irregular_search(target_lo=126_000, target_hi=130_000, ratio=5.6):
+    """Seed = first seed >= 0 whose compact rows fall in [target_lo, target_hi];
+    rho = the value on a 0.01 grid whose expanded/compact ratio is closest to ``ratio``."""
+    seed = 0
+    while True:
+        _, _, lens = _irregular_topology(seed, 0.0)
+        if target_lo <= sum(lens) <= target_hi:
+            break
+        seed += 1
+    best = None
+    for i in range(101):
+        rho = i / 100
+        p, f, l = _irregular_topology(seed, rho)
+        r = _expanded_rows(p, f, l) / sum(l)
+        if best is None or abs(r - ratio) < abs(best[1] - ratio):
+            best = (rho, r)
+    return seed, best[0], best[1]
+
+
+# Result of irregular_search() with the defaults (recorded so that construction is cheap;
+# tests re-run the search and check these values).
+IRREGULAR_SEED, IRREGULAR_RHO = 30, 0.92
+
+
+def irregular(seed: int | None = None, rho: float | None = None) -> Episode:
+    """64 root-to-leaf trajectories; edge lengths round(lognormal(7,1)) clipped to
+    [16,16384]; each new edge forks from the newest edge with probability rho, else from a
+    uniformly chosen earlier edge, at a uniform (unaligned) offset.  GQA 32/8, D=128, page 64."""
+    seed = IRREGULAR_SEED if seed is None else seed
+    rho = IRREGULAR_RHO if rho is None else rho
+    parents, forks, lens = _irregular_topology(seed, rho)
+    ep = Episode("irregular_tree", make_branches(parents, forks, lens), make_mounts([]),
+                 32, 8, 128, 64, seed)
+    ep.info = {"rho": rho, "expanded_rows": _expanded_rows(parents, forks, lens)}
+    return ep
+
+
+def mount_heavy(seed: int = 0, n_dags: int = 4) -> Episode:
+    """262,144 rows as 4 independent DAGs of 65,536 rows.  Each: 8192-row root; a
+    12,288-row producer worker forking at 8192 whose span [4096, 8192) is mounted by 32
+    reader workers of 1408 rows (forking at 8192, mount offset uniform in [1, 1407]).
+    GQA 16/4, D=128, page 64."""
+    (rng,) = _streams(seed, 1)
+    parents, forks, lens, mounts = [], [], [], []
+    for _ in range(n_dags):
+        base = len(parents)
+        parents += [-1, base]; forks += [0, 8192]; lens += [8192, 12288]
+        for _ in range(32):
+            rd = len(parents)
+            parents.append(base); forks.append(8192); lens.append(1408)
+            mounts.append((rd, int(rng.integers(1, 1408)), base + 1, 4096, 8192))
+    return Episode("mount_heavy", make_branches(parents, forks, lens), make_mounts(mounts),
+                   16, 4, 128, 64, seed)
+
+
+CONFIGS = {
+    0: tiny,
+    1: balanced,
+    2: commander_worker,
+    3: irregular,
+    4: mount_heavy,
+}
+
+
+def config(i: int) -> Episode:
+    return CONFIGS[i]()
+
+
+def scaled(i: int, factor: int, seed: int = 0) -> Episode:
+    """The shape of workload ``i`` with every length divided by ``factor`` (rounded, at least
+    a few rows), keeping heads/D/page: a parity case the oracle finishes in seconds."""
+    ep = CONFIGS[i]()
+    br = ep.branches.copy()
+    sc = lambda x: max(3, int(round(x / factor)))
+    new_len = [sc(int(l)) for l in br["length"]]
+    new_fork = []
+    for b in range(len(br)):
+        p = int(br["parent"][b])
+        if p < 0:
+            new_fork.append(0)
+        else:
+            f = int(br["fork_offset"][b])
+            nf = new_len[p] if f == int(br["length"][p]) else min(new_len[p], max(1, int(round(f / factor))))
+            new_fork.append(nf)
+    mts = []
+    for m in ep.mounts:
+        r, s = int(m["reader"]), int(m["source"])
+        e = new_len[s] if int(m["src_end"]) == int(br["length"][s]) else min(new_len[s], sc(int(m["src_end"])))
+        b0 = min(e - 1, int(round(int(m["src_begin"]) / factor)))
+        t = min(new_len[r] - 1, max(1, int(round(int(m["reader_offset"]) / factor))))
+        mts.append((r, t, s, b0, e))
+    out = Episode(f"{ep.name}/{factor}", make_branches(list(br["parent"]), new_fork, new_len),
+                  make_mounts(mts), ep.num_q_heads, ep.num_kv_heads, ep.head_dim, ep.page_size, seed)
+    return out
+
+
+def random_small(seed: int, max_branches: int = 7, max_len: int = 160, heads=(4, 1),
+                 head_dim: int = 64, page_size: int = 16, n_mounts: int | None = None,
+                 allow_zero_fork: bool = True, sibling_mounts_only: bool = False) -> Episode:
+    """A small random DAG for fuzzing: unaligned forks, stacked mounts, mounts only from
+    branches created earlier and not descending from the reader (so every mount is causal)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 7]))
+    nb = int(rng.integers(1, max_branches + 1))
+    parents, forks, lens = [-1], [0], [int(rng.integers(1, max_len + 1))]
+    for b in range(1, nb):
+        p = int(rng.integers(0, b))
+        lo = 0 if allow_zero_fork else 1
+        f = int(rng.integers(lo, lens[p] + 1))
+        parents.append(p); forks.append(f); lens.append(int(rng.integers(1, max_len + 1)))
+
+    def ancestors(b):
+        out = set()
+        while parents[b] >= 0:
+            b = parents[b]
+            out.add(b)
+        return out
+
+    nm = int(rng.integers(0, 4)) if n_mounts is None else n_mounts
+    mounts = []
+    for _ in range(nm * 4):
+        if len(mounts) >= nm or nb < 2:
+            break
+        r = int(rng.integers(1, nb))
+        s = int(rng.integers(0, r))            # created earlier than the reader
+        if sibling_mounts_only and (s in ancestors(r) or r in ancestors(s)):
+            continue
+        if r in ancestors(s):
+            continue
+        b0 = int(rng.integers(0, lens[s]))
+        e = int(rng.integers(b0 + 1, lens[s] + 1))
+        t = int(rng.integers(0, lens[r]))
+        mounts.append((r, t, s, b0, e))
+    return Episode(f"random_small/{seed}", make_branches(parents, forks, lens),
+                   make_mounts(mounts), heads[0], heads[1], head_dim, page_size, seed)
+
+
+# --------------------------------------------------------------------------------------
+# tensors and pool
+# --------------------------------------------------------------------------------------
+
+_DIST_SCALE = {
+    # (q scale, k scale, v scale, do scale) in units of 1/sqrt(D)
+    "config": (1.0, 1.0, 1.0, 1.0),       # N(0,1)/sqrt(D) everywhere: logits have std 1/D
+    "realistic": (math.sqrt(1.0), 1.0, 1.0, 1.0),   # q, k ~ N(0,1): logit std ~ 1
+    "sharp": (5.0, 1.0, 1.0, 1.0),        # q ~ 5 N(0,1), k ~ N(0,1): logit std ~ 5
+}
+
+
+def _normal_bf16(rng, shape, scale, chunk_rows=8192):
+    out = np.empty(shape, dtype=np.uint16)
+    s = np.float32(scale)
+    for r0 in range(0, shape[0], chunk_rows):
+        r1 = min(shape[0], r0 + chunk_rows)
+        x = rng.standard_normal((r1 - r0,) + tuple(shape[1:]), dtype=np.float32)
+        out[r0:r1] = f32_to_bf16_bits(x * s)
+    return out
+
+
+def make_tensors(ep: Episode, seed: int | None = None, dist: str = "config") -> Tensors:
+    seed = ep.seed if seed is None else seed
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 1001]))
+    N, Hq, Hkv, D = ep.n_rows, ep.num_q_heads, ep.num_kv_heads, ep.head_dim
+    qs, ks, vs, dos = _DIST_SCALE[dist]
+    base = 1.0 / math.sqrt(D)
+    if dist != "config":
+        q = _normal_bf16(rng, (N, Hq, D), qs)
+        k = _normal_bf16(rng, (N, Hkv, D), ks)
+    else:
+        q = _normal_bf16(rng, (N, Hq, D), base)
+        k = _normal_bf16(rng, (N, Hkv, D), base)
+    v = _normal_bf16(rng, (N, Hkv, D), base * vs)
+    do = _normal_bf16(rng, (N, Hq, D), base * dos)
+    return Tensors(q, k, v, do)
+
+
+def make_pool(ep: Episode, t: Tensors, seed: int | None = None, spare_frac: float = 0.05) -> Pool:
+    seed = ep.seed if seed is None else seed
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 2002]))
+    N, P, Hkv, D = ep.n_rows, ep.page_size, ep.num_kv_heads, ep.head_dim
+    n_logical = -(-N // P)
+    n_pages = n_logical + max(1, int(math.ceil(spare_frac * n_logical)))
+    page_table = rng.permutation(n_pages)[:n_logical].astype(np.int32)
+    k_pool = np.full((n_pages, P, Hkv, D), BF16_NAN, dtype=np.uint16)
+    v_pool = np.full((n_pages, P, Hkv, D), BF16_NAN, dtype=np.uint16)
+    # the logical pages: rows beyond N on the last page are zero
+    kp = np.zeros((n_logical * P, Hkv, D), dtype=np.uint16)
+    vp = np.zeros((n_logical * P, Hkv, D), dtype=np.uint16)
+    kp[:N] = t.k
+    vp[:N] = t.v
+    k_pool[page_table] = kp.reshape(n_logical, P, Hkv, D)
+    v_pool[page_table] = vp.reshape(n_logical, P, Hkv, D)
+    return Pool(page_table, k_pool, v_pool)
+
+
+def pool_rows(pool_arr: np.ndarray, page_table: np.ndarray, n_rows: int) -> np.ndarray:
+    """Gather compact rows [0, n_rows) back out of a paged pool [n_pages, P, ...]."""
+    P = pool_arr.shape[1]
+    g = pool_arr[page_table]
+    return g.reshape((g.shape[0] * P,) + pool_arr.shape[2:])[:n_rows]
