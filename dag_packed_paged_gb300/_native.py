@@ -1,0 +1,243 @@
+"""ctypes binding of libtreeattn (the C ABI in include/treeattn.h): argument marshalling only.
+
+Every step of the hot path runs in the library's kernels.  There is no fallback: if the
+shared library has not been built, importing the functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+from .build import LIB, INCLUDE
+
+TA_OK = 0
+TA_ERR_INVALID = -1
+TA_ERR_UNSUPPORTED = -2
+TA_ERR_NOMEM = -3
+TA_ERR_CUDA = -4
+TA_ERR_DEVICE_TIMEOUT = -5
+TA_CLAMP_MOUNTS = 0x1
+TA_PLAN_HOST_ONLY = 0x100
+
+HEADER = os.path.join(INCLUDE, "treeattn.h")
+
+
+class TreeAttnError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"treeattn error {code}: {msg}")
+        self.code = code
+
+
+class ta_branch(ctypes.Structure):
+    _fields_ = [("parent", ctypes.c_int32), ("fork_offset", ctypes.c_int32),
+                ("length", ctypes.c_int32), ("row_start", ctypes.c_int64)]
+
+
+class ta_mount(ctypes.Structure):
+    _fields_ = [("reader", ctypes.c_int32), ("reader_offset", ctypes.c_int32),
+                ("source", ctypes.c_int32), ("src_begin", ctypes.c_int32),
+                ("src_end", ctypes.c_int32)]
+
+
+class ta_config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("num_pages", ctypes.c_int64)]
+
+
+class ta_plan_stats(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int64), ("pairs", ctypes.c_int64),
+                ("fwd_flops", ctypes.c_double), ("bwd_flops", ctypes.c_double),
+                ("n_segments", ctypes.c_int64), ("n_blocks", ctypes.c_int64),
+                ("n_intervals", ctypes.c_int64), ("n_entries", ctypes.c_int64),
+                ("n_kv_tiles", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
+                ("n_partial_slots", ctypes.c_int64), ("block_rows", ctypes.c_int32),
+                ("tile_rows", ctypes.c_int32), ("bwd_workspace_bytes", ctypes.c_size_t),
+                ("plan_ms", ctypes.c_double)]
+
+
+_P32 = ctypes.POINTER(ctypes.c_int32)
+_P64 = ctypes.POINTER(ctypes.c_int64)
+
+
+class ta_plan_arrays(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int64), ("n_blocks", ctypes.c_int64),
+                ("n_intervals", ctypes.c_int64), ("n_entries", ctypes.c_int64),
+                ("n_chunks", ctypes.c_int64), ("pos_ids", _P32), ("blocks", _P32),
+                ("blk_iv_ptr", _P64), ("iv_lo", _P32), ("iv_hi", _P32), ("diag", _P32),
+                ("entries", _P32), ("t_entries", _P32), ("chunks", _P32), ("fwd_order", _P32)]
+
+
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/treeattn.h."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return re.findall(r"\b(tree_attn_\w+)\s*\(", txt)
+
+
+def lib():
+    """Load libtreeattn.so (built by dag_packed_paged_gb300.build / __graft_entry__.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise ImportError(f"{LIB} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    L.tree_attn_plan.argtypes = [vp, i32, vp, i32, vp, i64, ctypes.POINTER(ta_config), vp, vp,
+                                 ctypes.POINTER(vp)]
+    L.tree_attn_plan.restype = ctypes.c_int
+    L.tree_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+    L.tree_attn_fwd.restype = ctypes.c_int
+    L.tree_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.tree_attn_bwd.restype = ctypes.c_int
+    L.tree_attn_bwd_workspace_size.argtypes = [vp]
+    L.tree_attn_bwd_workspace_size.restype = sz
+    L.tree_attn_check.argtypes = [vp, vp]
+    L.tree_attn_check.restype = ctypes.c_int
+    L.tree_attn_plan_stats.argtypes = [vp, ctypes.POINTER(ta_plan_stats)]
+    L.tree_attn_plan_stats.restype = ctypes.c_int
+    L.tree_attn_plan_export.argtypes = [vp, ctypes.POINTER(ta_plan_arrays)]
+    L.tree_attn_plan_export.restype = ctypes.c_int
+    L.tree_attn_plan_destroy.argtypes = [vp]
+    L.tree_attn_plan_destroy.restype = None
+    L.tree_attn_last_error.argtypes = []
+    L.tree_attn_last_error.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def tree_attn_last_error() -> str:
+    return lib().tree_attn_last_error().decode()
+
+
+def _check(rc):
+    if rc != TA_OK:
+        raise TreeAttnError(rc, tree_attn_last_error())
+
+
+def _ptr(x):
+    """Device or host address of a torch tensor, numpy array, int or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return torch.cuda.current_stream().cuda_stream
+        except Exception:  # pragma: no cover
+            pass
+        return None
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+class Plan:
+    """Owns a ta_plan*; destroyed with tree_attn_plan_destroy."""
+
+    def __init__(self, handle, n_rows, pos_ids):
+        self.handle = handle
+        self.n_rows = n_rows
+        self.pos_ids = pos_ids
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib is not None:
+            _lib.tree_attn_plan_destroy(h)
+
+
+def tree_attn_plan(branches: np.ndarray, mounts: np.ndarray, page_table: np.ndarray, *,
+                   num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                   num_pages: int, softmax_scale: float = 0.0, flags: int = 0,
+                   stream=None) -> Plan:
+    """branches: structured array with fields parent, fork_offset, length, row_start (the
+    ta_branch layout); mounts: reader, reader_offset, source, src_begin, src_end."""
+    br = np.ascontiguousarray(branches)
+    mt = np.ascontiguousarray(mounts)
+    assert br.dtype.itemsize == ctypes.sizeof(ta_branch) and mt.dtype.itemsize == ctypes.sizeof(ta_mount)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    cfg = ta_config(num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale, flags, num_pages)
+    n_rows = int((br["row_start"] + br["length"]).max()) if len(br) else 0
+    pos = np.zeros(max(n_rows, 1), dtype=np.int32)
+    h = ctypes.c_void_p()
+    rc = lib().tree_attn_plan(br.ctypes.data if len(br) else None, len(br),
+                              mt.ctypes.data if len(mt) else None, len(mt),
+                              pt.ctypes.data if len(pt) else None, len(pt), ctypes.byref(cfg),
+                              pos.ctypes.data, _stream(stream) if not (flags & TA_PLAN_HOST_ONLY) else None,
+                              ctypes.byref(h))
+    _check(rc)
+    return Plan(h.value, n_rows, pos[:n_rows])
+
+
+def tree_attn_fwd(plan: Plan, q, k_pool, v_pool, o, lse, stream=None) -> None:
+    _check(lib().tree_attn_fwd(plan.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(o), _ptr(lse),
+                               _stream(stream)))
+
+
+def tree_attn_bwd(plan: Plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, workspace,
+                  ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().tree_attn_bwd(plan.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(o), _ptr(lse),
+                               _ptr(d_o), _ptr(dq), _ptr(dk_pool), _ptr(dv_pool), _ptr(workspace),
+                               int(ws_bytes), _stream(stream)))
+
+
+def tree_attn_bwd_workspace_size(plan: Plan) -> int:
+    return int(lib().tree_attn_bwd_workspace_size(plan.handle))
+
+
+def tree_attn_check(plan: Plan, stream=None) -> None:
+    _check(lib().tree_attn_check(plan.handle, _stream(stream)))
+
+
+def tree_attn_plan_stats(plan: Plan) -> dict:
+    st = ta_plan_stats()
+    _check(lib().tree_attn_plan_stats(plan.handle, ctypes.byref(st)))
+    return {f: getattr(st, f) for f, _ in ta_plan_stats._fields_}
+
+
+def tree_attn_plan_export(plan: Plan) -> dict:
+    """Copies of the plan's host arrays (see ta_plan_arrays)."""
+    a = ta_plan_arrays()
+    _check(lib().tree_attn_plan_export(plan.handle, ctypes.byref(a)))
+
+    def arr(p, n, dt=np.int32):
+        if n == 0:
+            return np.zeros(0, dtype=dt)
+        return np.ctypeslib.as_array(p, shape=(n,)).copy()
+
+    nb, ne = a.n_blocks, a.n_entries
+    return {
+        "n_rows": a.n_rows,
+        "pos_ids": arr(a.pos_ids, a.n_rows),
+        "blocks": arr(a.blocks, 4 * nb).reshape(nb, 4),
+        "blk_iv_ptr": arr(a.blk_iv_ptr, nb + 1, np.int64),
+        "iv_lo": arr(a.iv_lo, a.n_intervals),
+        "iv_hi": arr(a.iv_hi, a.n_intervals),
+        "diag": arr(a.diag, 2 * nb).reshape(nb, 2),
+        "entries": arr(a.entries, 4 * ne).reshape(ne, 4),
+        "t_entries": arr(a.t_entries, 4 * ne).reshape(ne, 4),
+        "chunks": arr(a.chunks, 4 * a.n_chunks).reshape(a.n_chunks, 4),
+        "fwd_order": arr(a.fwd_order, nb),
+    }
+
+
+def tree_attn_plan_destroy(plan: Plan) -> None:
+    h, plan.handle = plan.handle, None
+    if h:
+        lib().tree_attn_plan_destroy(h)

@@ -1,0 +1,363 @@
+// C ABI of libtreeattn: plan construction and upload, TMA descriptors, kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "kernels.h"
+#include "plan.h"
+
+namespace treeattn {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string &msg) { g_last_error = msg; }
+
+namespace {
+
+int cuda_fail(cudaError_t e, const char *what) {
+    set_error(std::string(what) + ": " + cudaGetErrorString(e));
+    return TA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A 2D bf16 view [rows][inner] with a row stride, boxes of box_inner x box_rows elements,
+// 128-byte swizzle (box_inner * 2 == 128), zero fill out of bounds.
+int make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+             uint32_t box_inner, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return TA_ERR_CUDA;
+    }
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed with code " + std::to_string(int(r)));
+        return TA_ERR_CUDA;
+    }
+    return TA_OK;
+}
+
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Tensor maps for Q-like [N, H, D] and the K/V pools.
+int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
+              CUtensorMap *tm_q, CUtensorMap *tm_k, CUtensorMap *tm_v) {
+    const HostPlan &h = plan->host;
+    const ta_config &c = h.cfg;
+    const uint32_t qb = std::min(h.block_rows, 128);
+    int rc = make_map(tm_q, q, uint64_t(c.num_q_heads) * c.head_dim, uint64_t(h.N),
+                      uint64_t(c.num_q_heads) * c.head_dim * 2, 64, qb);
+    if (rc) return rc;
+    const uint64_t pool_rows = uint64_t(c.num_pages) * c.page_size;
+    const uint64_t inner = uint64_t(c.num_kv_heads) * c.head_dim;
+    if ((rc = make_map(tm_k, k_pool, inner, pool_rows, inner * 2, 64, c.page_size))) return rc;
+    return make_map(tm_v, v_pool, inner, pool_rows, inner * 2, 64, c.page_size);
+}
+
+}  // namespace
+}  // namespace treeattn
+
+using namespace treeattn;
+
+extern "C" {
+
+const char *tree_attn_last_error(void) { return g_last_error.c_str(); }
+
+int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts, int32_t n_mounts,
+                   const int32_t *page_table, int64_t n_logical_pages, const ta_config *config,
+                   int32_t *pos_ids_out, void *stream, ta_plan **out) {
+    if (!out) {
+        set_error("out is NULL");
+        return TA_ERR_INVALID;
+    }
+    *out = nullptr;
+    ta_plan *plan = new (std::nothrow) ta_plan();
+    if (!plan) {
+        set_error("host allocation failed");
+        return TA_ERR_NOMEM;
+    }
+    int rc;
+    try {
+        rc = build_host_plan(branches, n_branches, mounts, n_mounts, page_table, n_logical_pages, config,
+                             plan->host);
+    } catch (const std::bad_alloc &) {
+        set_error("host allocation failed while planning");
+        rc = TA_ERR_NOMEM;
+    }
+    if (rc) {
+        delete plan;
+        return rc;
+    }
+    HostPlan &h = plan->host;
+    if (pos_ids_out && h.N > 0) std::memcpy(pos_ids_out, h.pos_ids.data(), sizeof(int32_t) * h.N);
+    {
+        const ta_config &c = h.cfg;
+        plan->ws_delta_bytes = align_up(sizeof(float) * size_t(c.num_q_heads) * size_t(h.N), 256);
+        plan->ws_bytes = plan->ws_delta_bytes +
+                         sizeof(float) * size_t(h.n_partial_slots) * c.num_kv_heads * 2 * kTileRows * c.head_dim;
+    }
+    if (h.cfg.flags & TA_PLAN_HOST_ONLY) {
+        *out = plan;
+        return TA_OK;
+    }
+
+    // one device buffer for every array the kernels read, plus status words
+    struct Part {
+        const void *src;
+        size_t bytes;
+        size_t off;
+    };
+    Part parts[8] = {
+        {h.blocks.data(), h.blocks.size() * 4, 0},   {h.entries.data(), h.entries.size() * 4, 0},
+        {h.t_entries.data(), h.t_entries.size() * 4, 0}, {h.chunks.data(), h.chunks.size() * 4, 0},
+        {h.fwd_order.data(), h.fwd_order.size() * 4, 0}, {h.reduce.data(), h.reduce.size() * 4, 0},
+        {h.page_table.data(), h.page_table.size() * 4, 0}, {nullptr, 64, 0},
+    };
+    size_t total = 0;
+    for (Part &p : parts) {
+        p.off = total;
+        total = align_up(total + std::max<size_t>(p.bytes, 16), 256);
+    }
+    std::vector<uint8_t> staging(total, 0);
+    for (Part &p : parts)
+        if (p.src && p.bytes) std::memcpy(staging.data() + p.off, p.src, p.bytes);
+    cudaError_t e = cudaGetDevice(&plan->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device);
+    if (e == cudaSuccess) e = cudaMalloc(&plan->d_buf, total);
+    if (e != cudaSuccess) {
+        delete plan;
+        return e == cudaErrorMemoryAllocation ? (set_error("device allocation failed"), TA_ERR_NOMEM)
+                                              : cuda_fail(e, "plan upload");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(plan->d_buf, staging.data(), total, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        cudaFree(plan->d_buf);
+        delete plan;
+        return cuda_fail(e, "plan upload");
+    }
+    uint8_t *d = static_cast<uint8_t *>(plan->d_buf);
+    plan->d_buf = d;
+    plan->d_bytes = total;
+    plan->d_blocks = reinterpret_cast<const int32_t *>(d + parts[0].off);
+    plan->d_entries = reinterpret_cast<const int32_t *>(d + parts[1].off);
+    plan->d_t_entries = reinterpret_cast<const int32_t *>(d + parts[2].off);
+    plan->d_chunks = reinterpret_cast<const int32_t *>(d + parts[3].off);
+    plan->d_fwd_order = reinterpret_cast<const int32_t *>(d + parts[4].off);
+    plan->d_reduce = reinterpret_cast<const int32_t *>(d + parts[5].off);
+    plan->d_page_table = reinterpret_cast<const int32_t *>(d + parts[6].off);
+    plan->d_status = reinterpret_cast<int32_t *>(d + parts[7].off);
+    *out = plan;
+    return TA_OK;
+}
+
+void tree_attn_plan_destroy(ta_plan *plan) {
+    if (!plan) return;
+    if (plan->d_buf) cudaFree(plan->d_buf);
+    delete plan;
+}
+
+size_t tree_attn_bwd_workspace_size(const ta_plan *plan) { return plan ? plan->ws_bytes : 0; }
+
+int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out) {
+    if (!plan || !out) {
+        set_error("NULL argument");
+        return TA_ERR_INVALID;
+    }
+    const HostPlan &h = plan->host;
+    std::memset(out, 0, sizeof(*out));
+    out->n_rows = h.N;
+    out->pairs = h.pairs;
+    out->fwd_flops = 4.0 * h.cfg.head_dim * h.cfg.num_q_heads * double(h.pairs);
+    out->bwd_flops = 10.0 * h.cfg.head_dim * h.cfg.num_q_heads * double(h.pairs);
+    out->n_segments = h.n_segments;
+    out->n_blocks = int64_t(h.blocks.size() / 4);
+    out->n_intervals = int64_t(h.iv_lo.size());
+    out->n_entries = int64_t(h.entries.size() / 4);
+    out->n_kv_tiles = (h.N + kTileRows - 1) / kTileRows;
+    out->n_chunks = int64_t(h.chunks.size() / 4);
+    out->n_partial_slots = h.n_partial_slots;
+    out->block_rows = h.block_rows;
+    out->tile_rows = kTileRows;
+    out->bwd_workspace_bytes = plan->ws_bytes;
+    out->plan_ms = h.plan_ms;
+    return TA_OK;
+}
+
+int tree_attn_plan_export(const ta_plan *plan, ta_plan_arrays *out) {
+    if (!plan || !out) {
+        set_error("NULL argument");
+        return TA_ERR_INVALID;
+    }
+    const HostPlan &h = plan->host;
+    out->n_rows = h.N;
+    out->n_blocks = int64_t(h.blocks.size() / 4);
+    out->n_intervals = int64_t(h.iv_lo.size());
+    out->n_entries = int64_t(h.entries.size() / 4);
+    out->n_chunks = int64_t(h.chunks.size() / 4);
+    out->pos_ids = h.pos_ids.data();
+    out->blocks = h.blocks.data();
+    out->blk_iv_ptr = h.blk_iv_ptr.data();
+    out->iv_lo = h.iv_lo.data();
+    out->iv_hi = h.iv_hi.data();
+    out->diag = h.diag.data();
+    out->entries = h.entries.data();
+    out->t_entries = h.t_entries.data();
+    out->chunks = h.chunks.data();
+    out->fwd_order = h.fwd_order.data();
+    return TA_OK;
+}
+
+static bool host_only(const ta_plan *plan) {
+    if (plan->d_buf) return false;
+    set_error("the plan was built with TA_PLAN_HOST_ONLY");
+    return true;
+}
+
+int tree_attn_check(const ta_plan *plan, void *stream) {
+    if (!plan) {
+        set_error("plan is NULL");
+        return TA_ERR_INVALID;
+    }
+    if (host_only(plan)) return TA_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int32_t st[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (st[0] | st[1] | st[2] | st[3]) {
+        cudaMemset(plan->d_status, 0, sizeof(st));
+        cudaDeviceSynchronize();
+        set_error("a bounded device-side wait expired; outputs of the affected launches are invalid");
+        return TA_ERR_DEVICE_TIMEOUT;
+    }
+    return TA_OK;
+}
+
+int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool, void *o,
+                  float *lse, void *stream) {
+    if (!plan) {
+        set_error("plan is NULL");
+        return TA_ERR_INVALID;
+    }
+    const HostPlan &h = plan->host;
+    if (h.N == 0) return TA_OK;
+    if (host_only(plan)) return TA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(lse)) {
+        set_error("tree_attn_fwd: NULL or misaligned (16-byte) pointer");
+        return TA_ERR_INVALID;
+    }
+    CUtensorMap tm_q, tm_k, tm_v;
+    int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &tm_k, &tm_v);
+    if (rc) return rc;
+    FwdParams p{};
+    p.blocks = plan->d_blocks;
+    p.entries = plan->d_entries;
+    p.order = plan->d_fwd_order;
+    p.page_table = plan->d_page_table;
+    p.n_logical_pages = int32_t(h.n_logical_pages);
+    p.num_pages = int32_t(h.cfg.num_pages);
+    p.page_size = h.cfg.page_size;
+    p.N = int32_t(h.N);
+    p.Hq = h.cfg.num_q_heads;
+    p.Hkv = h.cfg.num_kv_heads;
+    p.G = h.G;
+    p.R = h.block_rows;
+    p.scale_log2 = h.scale * 1.4426950408889634f;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.status = plan->d_status;
+    cudaError_t e = launch_fwd(h.cfg.head_dim, tm_q, tm_k, tm_v, p, int(h.blocks.size() / 4),
+                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
+    return TA_OK;
+}
+
+int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool, const void *o,
+                  const float *lse, const void *d_o, float *dq, float *dk_pool, float *dv_pool, void *workspace,
+                  size_t ws_bytes, void *stream) {
+    if (!plan) {
+        set_error("plan is NULL");
+        return TA_ERR_INVALID;
+    }
+    const HostPlan &h = plan->host;
+    if (h.N == 0) return TA_OK;
+    if (host_only(plan)) return TA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(d_o) || !aligned16(dq) || !aligned16(dk_pool) || !aligned16(dv_pool)) {
+        set_error("tree_attn_bwd: NULL or misaligned (16-byte) pointer");
+        return TA_ERR_INVALID;
+    }
+    if (ws_bytes < plan->ws_bytes || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        set_error("tree_attn_bwd: workspace too small or not 256-byte aligned");
+        return TA_ERR_INVALID;
+    }
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &tm_k, &tm_v);
+    if (rc) return rc;
+    const ta_config &c = h.cfg;
+    if ((rc = make_map(&tm_do, d_o, uint64_t(c.num_q_heads) * c.head_dim, uint64_t(h.N),
+                       uint64_t(c.num_q_heads) * c.head_dim * 2, 64, std::min(h.block_rows, 128))))
+        return rc;
+    BwdParams p{};
+    p.blocks = plan->d_blocks;
+    p.entries = plan->d_entries;
+    p.t_entries = plan->d_t_entries;
+    p.chunks = plan->d_chunks;
+    p.reduce = plan->d_reduce;
+    p.order = plan->d_fwd_order;
+    p.page_table = plan->d_page_table;
+    p.n_logical_pages = int32_t(h.n_logical_pages);
+    p.num_pages = int32_t(c.num_pages);
+    p.page_size = c.page_size;
+    p.N = int32_t(h.N);
+    p.Hq = c.num_q_heads;
+    p.Hkv = c.num_kv_heads;
+    p.G = h.G;
+    p.R = h.block_rows;
+    p.scale = h.scale;
+    p.scale_log2 = h.scale * 1.4426950408889634f;
+    p.o = static_cast<const __nv_bfloat16 *>(o);
+    p.d_o = static_cast<const __nv_bfloat16 *>(d_o);
+    p.lse = lse;
+    p.delta = static_cast<float *>(workspace);
+    p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan->ws_delta_bytes);
+    p.dq = dq;
+    p.dk_pool = dk_pool;
+    p.dv_pool = dv_pool;
+    p.status = plan->d_status + 1;
+    cudaError_t e = launch_bwd(c.head_dim, tm_q, tm_k, tm_v, tm_do, p, int(h.blocks.size() / 4),
+                               int(h.chunks.size() / 4), int(h.reduce.size() / 4), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree_attn_bwd launch");
+    return TA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,549 @@
+// Backward kernels for tree/DAG-packed paged attention (sm_103a, tcgen05 + TMA).
+//
+// With P = softmax over vis(r) recomputed from the saved logsumexp and delta = <dO, O>:
+//   dS = P * (dO V^T - delta),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO
+// (the adjoint of the forward in Octopus arXiv 2611.06956 Section 3.3 Eq. 4; gradients of a
+// shared prefix row or a mounted row are summed over all of its readers -- Octopus Section 3.4
+// "differentiable mount edges", HARTS arXiv 2608.28158 Section 3.4 gather backward).
+//
+// Four launches:
+//   delta_kernel   delta[h, r] = <dO[r,h], O[r,h]>                           (HBM-bound)
+//   dq_kernel      query-major: one CTA per (query block, KV head, 128-lane query tile);
+//                  walks the block's key-tile entries like the forward
+//   dkdv_kernel    key-major: one CTA per (key-tile chunk, KV head); walks the query blocks
+//                  that read the tile (the plan's transpose), both 128-lane query tiles each;
+//                  dK and dV accumulate in TMEM and are written once -- to the pool, or to a
+//                  partial slot when the tile's readers were split into several chunks
+//   reduce_kernel  sums each split tile's partial slots in a fixed order (deterministic)
+#include "kernels.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace treeattn {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------------------ delta
+template <int D>
+__global__ void __launch_bounds__(256) delta_kernel(const BwdParams p) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int total = p.N * p.Hq;
+    if (warp >= total) return;
+    const int r = warp / p.Hq, h = warp % p.Hq;
+    const size_t base = (static_cast<size_t>(r) * p.Hq + h) * D;
+    float acc = 0.f;
+    constexpr int V = D / 32;   // elements per lane
+    const __nv_bfloat16 *a = p.d_o + base + lane * V;
+    const __nv_bfloat16 *b = p.o + base + lane * V;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc += __bfloat162float(a[i]) * __bfloat162float(b[i]);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) p.delta[static_cast<size_t>(h) * p.N + r] = acc;
+}
+
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *tm, int tile, int g, int D,
+                                             const int32_t *page_table, int n_logical, int num_pages, int P,
+                                             uint32_t bar) {
+    const int pages = kTileRows / P;
+    for (int i = 0; i < pages; ++i) {
+        const int l = tile * pages + i;
+        const int y = l < n_logical ? __ldg(page_table + l) * P : num_pages * P;
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(dst + c * (kTileRows * 128) + i * P * 128, tm, g * D + c * 64, y, bar);
+    }
+}
+
+// One 128-lane query tile t of a block: rows (head, row) flattened as m = hl * R + rl.
+__device__ __forceinline__ void load_q_tile(uint32_t dst, const CUtensorMap *tm, int t, int g, int G, int R,
+                                            int D, int q_row0, uint32_t bar) {
+    const int QB = R < 128 ? R : 128;
+    for (int b = 0; b < 128 / QB; ++b) {
+        const int m0 = 128 * t + b * QB, hl = m0 / R, r0 = m0 % R;
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(dst + c * 16384 + b * QB * 128, tm, (g * G + hl) * D + c * 64, q_row0 + r0, bar);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t sB, uint32_t idesc) {
+    // D[128 x 128] = A[128 x D] * B[128 x D]^T, both K-major 128-byte-swizzled tiles
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
+        mma_ss(d_tmem, sdesc_sw128(sA + koff, 16, 1024), sdesc_sw128(sB + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc, bool acc) {
+    // D[128 x D] (+)= A[128 x 128] (bf16 in TMEM) * B[128 x D] (MN-major tile in smem)
+#pragma unroll
+    for (int kk = 0; kk < kTileRows / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(sB + kk * 16 * 128, kTileRows * 128, 1024), idesc,
+               (acc || kk > 0) ? 1u : 0u);
+}
+
+// ------------------------------------------------------------------------------ dQ
+constexpr int kDqThreads = 192;   // warps 0-3 elementwise, 4 TMA, 5 MMA
+constexpr int kStages = 2;
+
+template <int D>
+struct DqLayout {
+    static constexpr int kTile = 128 * D * 2;
+    static constexpr int q_off = 0;
+    static constexpr int do_off = q_off + kTile;
+    static constexpr int k_off = do_off + kTile;
+    static constexpr int v_off = k_off + kStages * kTile;
+    static constexpr int bar_off = v_off + kStages * kTile;
+    static constexpr int n_bars = 1 + 4 * kStages + 3;
+    static constexpr int misc_off = bar_off + n_bars * 8;
+    static constexpr int bytes = misc_off + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDqThreads, 1)
+dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+    using L = DqLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int unit = blockIdx.x >> 1, t = blockIdx.x & 1;
+    const int qb = __ldg(p.order + unit / p.Hkv), g = unit % p.Hkv;
+    const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
+    const int e0 = __ldg(p.blocks + 4 * qb + 2), E = __ldg(p.blocks + 4 * qb + 3) - e0;
+    const int4 *entries = reinterpret_cast<const int4 *>(p.entries) + e0;
+
+    const uint32_t sQ = sbase + L::q_off, sDO = sbase + L::do_off, sK = sbase + L::k_off, sV = sbase + L::v_off;
+    auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
+    const uint32_t q_full = bar(0);
+    auto k_full = [&](int s) { return bar(1 + s); };
+    auto k_empty = [&](int s) { return bar(1 + kStages + s); };
+    auto v_full = [&](int s) { return bar(1 + 2 * kStages + s); };
+    auto v_empty = [&](int s) { return bar(1 + 3 * kStages + s); };
+    const uint32_t s_full = bar(1 + 4 * kStages), p_full = bar(2 + 4 * kStages), o_full = bar(3 + 4 * kStages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_full, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // TMEM columns: S [0,128) | dP [128,256) (dS overwrites its first half) | dQ [256, 256+D)
+    constexpr uint32_t cS = 0, cDP = 128, cDQ = 256;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(q_full, 2 * L::kTile);
+            load_q_tile(sQ, &tm_q, t, g, p.G, p.R, D, q_row0, q_full);
+            load_q_tile(sDO, &tm_do, t, g, p.G, p.R, D, q_row0, q_full);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < E; ++j) {
+                const int tile = __ldg(&entries[j].x), s = j % kStages;
+                if (j >= kStages && !mbar_wait(k_empty(s), ((j / kStages) - 1) & 1, abort, p.status)) break;
+                mbar_arrive_expect_tx(k_full(s), L::kTile);
+                load_kv_tile(sK + s * L::kTile, &tm_k, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages,
+                             p.page_size, k_full(s));
+                k_issued = j + 1;
+                if (j >= kStages && !mbar_wait(v_empty(s), ((j / kStages) - 1) & 1, abort, p.status)) break;
+                mbar_arrive_expect_tx(v_full(s), L::kTile);
+                load_kv_tile(sV + s * L::kTile, &tm_v, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages,
+                             p.page_size, v_full(s));
+                v_issued = j + 1;
+            }
+            for (int d = (k_issued > kStages ? k_issued - kStages : 0); d < k_issued; ++d)
+                mbar_wait(k_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
+            for (int d = (v_issued > kStages ? v_issued - kStages : 0); d < v_issued; ++d)
+                mbar_wait(v_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
+            mbar_wait(q_full, 0, nullptr, p.status);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, kTileRows, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
+            bool ok = E > 0 && mbar_wait(q_full, 0, abort, p.status);
+            for (int j = 0; ok && j < E; ++j) {
+                const int s = j % kStages, ph = (j / kStages) & 1;
+                if (!(ok = mbar_wait(k_full(s), ph, abort, p.status))) break;
+                if (!(ok = mbar_wait(v_full(s), ph, abort, p.status))) break;
+                tc_fence_after();
+                issue_qk<D>(tmem + cS, sQ, sK + s * L::kTile, idesc_s);
+                issue_qk<D>(tmem + cDP, sDO, sV + s * L::kTile, idesc_s);
+                mma_commit(s_full);
+                mma_commit(v_empty(s));
+                if (!(ok = mbar_wait(p_full, j & 1, abort, p.status))) break;
+                tc_fence_after();
+                issue_tn<D>(tmem + cDQ, tmem + cDP, sK + s * L::kTile, idesc_o, j > 0);
+                mma_commit(k_empty(s));
+            }
+            mma_commit(o_full);
+            mbar_wait(o_full, 0, nullptr, p.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- elementwise (warps 0-3)
+        const int q4 = warp;
+        const int m_flat = 128 * t + 32 * q4 + lane;
+        const int hl = m_flat / p.R, rl = m_flat % p.R;
+        const int r_abs = q_row0 + rl, h = g * p.G + hl;
+        const bool valid = rl < n_rows;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const float sl2 = p.scale_log2;
+        const float lse2 = valid ? __ldg(p.lse + static_cast<size_t>(h) * p.N + r_abs) * kLog2e : INFINITY;
+        const float delta = valid ? p.delta[static_cast<size_t>(h) * p.N + r_abs] : 0.f;
+        bool ok = true;
+        for (int j = 0; j < E; ++j) {
+            const int4 e = __ldg(&entries[j]);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const int j0 = e.x * kTileRows;
+            const int hi = (e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z;
+#pragma unroll
+            for (int c = 0; c < kTileRows / 32; ++c) {
+                uint32_t sv[32], dpv[32], ds[16];
+                tmem_ld32(tmem + lane_off + cS + 32 * c, sv);
+                tmem_ld32(tmem + lane_off + cDP + 32 * c, dpv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float pr[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int jj = j0 + 32 * c + 2 * i + u;
+                        const float pv = ex2(fmaf(__uint_as_float(sv[2 * i + u]), sl2, -lse2));
+                        const bool vis = e.w == 0 || (jj >= e.y && jj < hi);
+                        pr[u] = vis ? pv * (__uint_as_float(dpv[2 * i + u]) - delta) : 0.f;
+                    }
+                    ds[i] = pack_bf16(pr[0], pr[1]);
+                }
+                tmem_st16(tmem + lane_off + cDP + 16 * c, ds);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
+        if (ok) {
+            tc_fence_after();
+            float *dst = p.dq + (static_cast<size_t>(r_abs) * p.Hq + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + cDQ + 32 * c, v);
+                tmem_wait_ld();
+                if (valid) {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(v[4 * i]) * p.scale, __uint_as_float(v[4 * i + 1]) * p.scale,
+                                            __uint_as_float(v[4 * i + 2]) * p.scale, __uint_as_float(v[4 * i + 3]) * p.scale);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------------ dK, dV
+constexpr int kKvThreads = 192;   // warps 0-3 elementwise, 4 loads, 5 MMA
+
+template <int D>
+struct DkvLayout {
+    static constexpr int kTile = 128 * D * 2;
+    static constexpr int k_off = 0;
+    static constexpr int v_off = k_off + kTile;
+    static constexpr int q_off = v_off + kTile;                 // stage s: Q at q_off + s*2*kTile, dO after it
+    static constexpr int lse_off = q_off + kStages * 2 * kTile; // stage s: 128 lse2 + 128 delta + 128 rows
+    static constexpr int bar_off = lse_off + kStages * 3 * 128 * 4;
+    static constexpr int n_bars = 1 + 2 * kStages + 3;
+    static constexpr int misc_off = bar_off + n_bars * 8;
+    static constexpr int bytes = misc_off + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kKvThreads, 1)
+dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+    using L = DkvLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int ci = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+    const int tile = __ldg(p.chunks + 4 * ci), a0 = __ldg(p.chunks + 4 * ci + 1);
+    const int n_ent = __ldg(p.chunks + 4 * ci + 2) - a0, slot = __ldg(p.chunks + 4 * ci + 3);
+    const int4 *tents = reinterpret_cast<const int4 *>(p.t_entries) + a0;
+    const int U = 2 * n_ent;   // (entry, query tile) units
+
+    const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off;
+    auto sQ = [&](int s) { return sbase + L::q_off + s * 2 * L::kTile; };
+    auto sDO = [&](int s) { return sbase + L::q_off + s * 2 * L::kTile + L::kTile; };
+    float *lse_s = reinterpret_cast<float *>(smem + L::lse_off);     // [stage][3][128]
+    auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
+    const uint32_t kv_full = bar(0);
+    auto qd_full = [&](int s) { return bar(1 + s); };
+    auto qd_empty = [&](int s) { return bar(1 + kStages + s); };
+    const uint32_t s_full = bar(1 + 2 * kStages), p_full = bar(2 + 2 * kStages), o_full = bar(3 + 2 * kStages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < kStages; ++s) { mbar_init(qd_full(s), 1); mbar_init(qd_empty(s), 1); }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_full, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // TMEM columns: S^T [0,128) (P^T overwrites its first half) | dP^T [128,256) (dS^T likewise)
+    //               | dV [256, 256+D) | dK [256+D, 256+2D)
+    constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------------- loads (whole warp)
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+            load_kv_tile(sK, &tm_k, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages, p.page_size, kv_full);
+            load_kv_tile(sV, &tm_v, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages, p.page_size, kv_full);
+        }
+        int issued = 0;
+        for (int u = 0; u < U; ++u) {
+            const int s = u % kStages, t = u & 1;
+            bool ok = true;
+            if (lane == 0 && u >= kStages) ok = mbar_wait(qd_empty(s), ((u / kStages) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            const int4 te = __ldg(&tents[u >> 1]);
+            const int qb = te.x;
+            const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
+            float *ls = lse_s + s * 3 * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = lane + 32 * i, m_flat = 128 * t + m;
+                const int hl = m_flat / p.R, rl = m_flat % p.R, h = g * p.G + hl;
+                const bool valid = rl < n_rows;
+                const size_t idx = static_cast<size_t>(h) * p.N + q_row0 + rl;
+                ls[m] = valid ? __ldg(p.lse + idx) * kLog2e : INFINITY;      // +inf: P = 0 for padding rows
+                ls[128 + m] = valid ? p.delta[idx] : 0.f;
+                reinterpret_cast<int *>(ls)[256 + m] = q_row0 + rl;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(qd_full(s), 2 * L::kTile);
+                load_q_tile(sQ(s), &tm_q, t, g, p.G, p.R, D, q_row0, qd_full(s));
+                load_q_tile(sDO(s), &tm_do, t, g, p.G, p.R, D, q_row0, qd_full(s));
+            }
+            issued = u + 1;
+        }
+        if (lane == 0) {
+            for (int d = (issued > kStages ? issued - kStages : 0); d < issued; ++d)
+                mbar_wait(qd_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
+            mbar_wait(kv_full, 0, nullptr, p.status);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
+            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status);
+            for (int u = 0; ok && u < U; ++u) {
+                const int s = u % kStages;
+                if (!(ok = mbar_wait(qd_full(s), (u / kStages) & 1, abort, p.status))) break;
+                tc_fence_after();
+                issue_qk<D>(tmem + cS, sK, sQ(s), idesc_s);       // S^T = K Q^T
+                issue_qk<D>(tmem + cDP, sV, sDO(s), idesc_s);     // dP^T = V dO^T
+                mma_commit(s_full);
+                if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
+                tc_fence_after();
+                issue_tn<D>(tmem + cDV, tmem + cS, sDO(s), idesc_o, u > 0);    // dV += P^T dO
+                issue_tn<D>(tmem + cDK, tmem + cDP, sQ(s), idesc_o, u > 0);    // dK += dS^T Q
+                mma_commit(qd_empty(s));
+            }
+            mma_commit(o_full);
+            mbar_wait(o_full, 0, nullptr, p.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- elementwise (warps 0-3)
+        const int q4 = warp;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const int row = 32 * q4 + lane;                 // key row within the tile
+        const int jj = tile * kTileRows + row;          // its compact row
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int u = 0; u < U; ++u) {
+            const int s = u % kStages;
+            const int4 te = __ldg(&tents[u >> 1]);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, abort, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const float *ls = lse_s + s * 3 * 128;
+            const int *rs = reinterpret_cast<const int *>(ls) + 256;
+            const bool row_in = jj >= te.y && jj < te.z;
+            const bool causal = (te.w & kEntryCausal) != 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dpv[32], pk[16], dk[16];
+                tmem_ld32(tmem + lane_off + cS + 32 * c, sv);
+                tmem_ld32(tmem + lane_off + cDP + 32 * c, dpv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float pr[2], dr[2];
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int m = 32 * c + 2 * i + w;
+                        float pv = ex2(fmaf(__uint_as_float(sv[2 * i + w]), sl2, -ls[m]));
+                        if (!row_in || (causal && jj > rs[m])) pv = 0.f;
+                        pr[w] = pv;
+                        dr[w] = pv * (__uint_as_float(dpv[2 * i + w]) - ls[128 + m]);
+                    }
+                    pk[i] = pack_bf16(pr[0], pr[1]);
+                    dk[i] = pack_bf16(dr[0], dr[1]);
+                }
+                tmem_st16(tmem + lane_off + cS + 16 * c, pk);
+                tmem_st16(tmem + lane_off + cDP + 16 * c, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
+        if (ok) {
+            tc_fence_after();
+            float *dk_dst, *dv_dst;
+            bool write = true;
+            if (slot >= 0) {
+                float *base = p.partials + (static_cast<size_t>(slot) * p.Hkv + g) * 2 * kTileRows * D;
+                dk_dst = base + static_cast<size_t>(row) * D;
+                dv_dst = base + static_cast<size_t>(kTileRows + row) * D;
+            } else {
+                write = jj < p.N;
+                const int l = jj / p.page_size;
+                const size_t prow = write ? static_cast<size_t>(__ldg(p.page_table + l)) * p.page_size + jj % p.page_size : 0;
+                dk_dst = p.dk_pool + (prow * p.Hkv + g) * D;
+                dv_dst = p.dv_pool + (prow * p.Hkv + g) * D;
+            }
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t kv[32], vv[32];
+                tmem_ld32(tmem + lane_off + cDK + 32 * c, kv);
+                tmem_ld32(tmem + lane_off + cDV + 32 * c, vv);
+                tmem_wait_ld();
+                if (write) {
+                    float4 *k4 = reinterpret_cast<float4 *>(dk_dst + 32 * c);
+                    float4 *v4 = reinterpret_cast<float4 *>(dv_dst + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        k4[i] = make_float4(__uint_as_float(kv[4 * i]) * p.scale, __uint_as_float(kv[4 * i + 1]) * p.scale,
+                                            __uint_as_float(kv[4 * i + 2]) * p.scale, __uint_as_float(kv[4 * i + 3]) * p.scale);
+                        v4[i] = make_float4(__uint_as_float(vv[4 * i]), __uint_as_float(vv[4 * i + 1]),
+                                            __uint_as_float(vv[4 * i + 2]), __uint_as_float(vv[4 * i + 3]));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------------ reduce
+// One CTA per (split tile, KV head): dK and dV of every row = sum of the tile's partial
+// slots in slot order, written through the page table.
+template <int D>
+__global__ void __launch_bounds__(256) reduce_kernel(const BwdParams p) {
+    const int ri = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+    const int tile = __ldg(p.reduce + 4 * ri), s0 = __ldg(p.reduce + 4 * ri + 1), ns = __ldg(p.reduce + 4 * ri + 2);
+    constexpr int V4 = D / 4;
+    for (int idx = threadIdx.x; idx < 2 * kTileRows * V4; idx += blockDim.x) {
+        const int which = idx / (kTileRows * V4), rem = idx % (kTileRows * V4);
+        const int row = rem / V4, c4 = rem % V4;
+        const int jj = tile * kTileRows + row;
+        if (jj >= p.N) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < ns; ++s) {
+            const float4 v = reinterpret_cast<const float4 *>(
+                p.partials + ((static_cast<size_t>(s0 + s) * p.Hkv + g) * 2 + which) * kTileRows * D)[row * V4 + c4];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const size_t prow = static_cast<size_t>(__ldg(p.page_table + jj / p.page_size)) * p.page_size + jj % p.page_size;
+        float *dst = (which == 0 ? p.dk_pool : p.dv_pool) + (prow * p.Hkv + g) * D;
+        reinterpret_cast<float4 *>(dst)[c4] = acc;
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                         const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
+                         cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.N) * p.Hq;
+    delta_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::bytes);
+    if (e != cudaSuccess) return e;
+    dq_kernel<D><<<n_blocks * p.Hkv * 2, kDqThreads, DqLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::bytes);
+    if (e != cudaSuccess) return e;
+    dkdv_kernel<D><<<n_chunks * p.Hkv, kKvThreads, DkvLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (n_reduce > 0) {
+        reduce_kernel<D><<<n_reduce * p.Hkv, 256, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
+                       cudaStream_t stream) {
+    if (D == 64) return launch_bwd_d<64>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream);
+    return launch_bwd_d<128>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream);
+}
+
+}  // namespace treeattn

@@ -1,0 +1,326 @@
+// Forward kernel: tree/DAG-packed attention over a paged KV pool (sm_103a, tcgen05 + TMA).
+//
+// Computes, for every row r of one query block and the G query heads of one KV head g,
+//   O[r,h] = sum_{j in vis(r)} softmax_j(scale q[r,h].k[j,g]) v[j,g],   lse[h,r] = ln sum exp
+// (Octopus arXiv 2611.06956 Section 3.3 Eq. 4 with the rectangular causal alignment after it;
+// HARTS arXiv 2608.28158 Section 4.2 Eq. 21-22), visiting only the key tiles the plan lists
+// for the block and masking rows outside each entry's [lo, hi) and, on diagonal tiles, above
+// the query row.
+//
+// One CTA = one query block (R rows x G heads = 256 query rows of the MMA, two 128-lane
+// tiles) x one KV head.  Warp roles:
+//   warps 0-3  softmax for query tile 0 (one TMEM lane = one (row, head) per thread)
+//   warps 4-7  softmax for query tile 1
+//   warp 8     TMA producer: Q once, then K and V tiles page by page (box = one page)
+//   warp 9     tcgen05 MMA issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P read from TMEM
+// TMEM (512 columns): S0 | S1 | O0 | O1; P_t (bf16 pairs) overwrites the first half of S_t.
+// The two query tiles ping-pong so that one tile's softmax overlaps the other tile's MMAs.
+// The running max is rescaled lazily (only when it grows by more than 2^8).
+#include <cfloat>
+
+#include "kernels.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace treeattn {
+
+namespace {
+
+constexpr int kKS = 2;           // K stages
+constexpr int kVS = 2;           // V stages
+constexpr int kThreads = 320;
+
+template <int D>
+struct FwdLayout {
+    static constexpr int kQTile = 128 * D * 2;            // bytes of one 128-row Q tile
+    static constexpr int kKV = kTileRows * D * 2;          // bytes of one K or V tile
+    static constexpr int q_off = 0;
+    static constexpr int k_off = q_off + 2 * kQTile;
+    static constexpr int v_off = k_off + kKS * kKV;
+    static constexpr int bar_off = v_off + kVS * kKV;
+    static constexpr int n_bars = 1 + 2 * kKS + 2 * kVS + 2 + 2 + 1;
+    static constexpr int misc_off = bar_off + n_bars * 8;
+    static constexpr int bytes = misc_off + 16 + 1024;     // + alignment slack
+};
+
+// TMA: one K or V tile (kTileRows rows of KV head g) of logical tile `tile`, page by page.
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *tm, int tile, int g,
+                                             int D, const int32_t *page_table, int n_logical,
+                                             int num_pages, int P, uint32_t bar) {
+    const int pages = kTileRows / P;
+    for (int i = 0; i < pages; ++i) {
+        const int l = tile * pages + i;
+        const int y = l < n_logical ? __ldg(page_table + l) * P : num_pages * P;   // past the end: zero fill
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(dst + c * (kTileRows * 128) + i * P * 128, tm, g * D + c * 64, y, bar);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using L = FwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int qb = __ldg(p.order + blockIdx.x / p.Hkv);
+    const int g = blockIdx.x % p.Hkv;
+    const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
+    const int e0 = __ldg(p.blocks + 4 * qb + 2), E = __ldg(p.blocks + 4 * qb + 3) - e0;
+    const int4 *entries = reinterpret_cast<const int4 *>(p.entries) + e0;
+
+    const uint32_t sQ = sbase + L::q_off, sK = sbase + L::k_off, sV = sbase + L::v_off;
+    auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
+    const uint32_t q_full = bar(0);
+    auto k_full = [&](int s) { return bar(1 + s); };
+    auto k_empty = [&](int s) { return bar(1 + kKS + s); };
+    auto v_full = [&](int s) { return bar(1 + 2 * kKS + s); };
+    auto v_empty = [&](int s) { return bar(1 + 2 * kKS + kVS + s); };
+    auto s_full = [&](int t) { return bar(1 + 2 * kKS + 2 * kVS + t); };
+    auto p_full = [&](int t) { return bar(3 + 2 * kKS + 2 * kVS + t); };
+    const uint32_t o_full = bar(5 + 2 * kKS + 2 * kVS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kKS; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
+        for (int s = 0; s < kVS; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
+        for (int t = 0; t < 2; ++t) { mbar_init(s_full(t), 1); mbar_init(p_full(t), 128); }
+        mbar_init(o_full, 1);
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const int R = p.R, QB = R < 128 ? R : 128;
+            mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
+            for (int t = 0; t < 2; ++t)
+                for (int b = 0; b < 128 / QB; ++b) {
+                    const int m0 = 128 * t + b * QB, hl = m0 / R, r0 = m0 % R;
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sQ + t * L::kQTile + c * 16384 + b * QB * 128, &tm_q,
+                                    (g * p.G + hl) * D + c * 64, q_row0 + r0, q_full);
+                }
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < E; ++j) {
+                const int tile = __ldg(&entries[j].x);
+                const int ks = j % kKS, vs = j % kVS;
+                if (j >= kKS && !mbar_wait(k_empty(ks), ((j / kKS) - 1) & 1, abort, p.status)) break;
+                mbar_arrive_expect_tx(k_full(ks), L::kKV);
+                load_kv_tile(sK + ks * L::kKV, &tm_k, tile, g, D, p.page_table, p.n_logical_pages,
+                             p.num_pages, p.page_size, k_full(ks));
+                k_issued = j + 1;
+                if (j >= kVS && !mbar_wait(v_empty(vs), ((j / kVS) - 1) & 1, abort, p.status)) break;
+                mbar_arrive_expect_tx(v_full(vs), L::kKV);
+                load_kv_tile(sV + vs * L::kKV, &tm_v, tile, g, D, p.page_table, p.n_logical_pages,
+                             p.num_pages, p.page_size, v_full(vs));
+                v_issued = j + 1;
+            }
+            // never leave the CTA with copies in flight: wait for the last phase of each stage
+            for (int d = (k_issued > kKS ? k_issued - kKS : 0); d < k_issued; ++d)
+                mbar_wait(k_full(d % kKS), (d / kKS) & 1, nullptr, p.status);
+            for (int d = (v_issued > kVS ? v_issued - kVS : 0); d < v_issued; ++d)
+                mbar_wait(v_full(d % kVS), (d / kVS) & 1, nullptr, p.status);
+            mbar_wait(q_full, 0, nullptr, p.status);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, kTileRows, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
+            auto issue_s = [&](int t, int ks) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(sQ + t * L::kQTile + koff, 16, 1024);
+                    const uint64_t b = sdesc_sw128(sK + ks * L::kKV + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_ss(tmem + t * 128, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int vs, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(sV + vs * L::kKV + kk * 16 * 128, kTileRows * 128, 1024);
+                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = E > 0 && mbar_wait(q_full, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                mma_commit(s_full(0));
+                issue_s(1, 0);
+                mma_commit(s_full(1));
+                mma_commit(k_empty(0));
+            }
+            for (int j = 0; ok && j < E; ++j) {
+                const int vs = j % kVS, ks = (j + 1) % kKS;
+                if (!(ok = mbar_wait(v_full(vs), (j / kVS) & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
+                tc_fence_after();
+                issue_pv(0, vs, j > 0);
+                if (j + 1 < E) {
+                    if (!(ok = mbar_wait(k_full(ks), ((j + 1) / kKS) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    issue_s(0, ks);
+                    mma_commit(s_full(0));
+                }
+                if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
+                tc_fence_after();
+                issue_pv(1, vs, j > 0);
+                mma_commit(v_empty(vs));
+                if (j + 1 < E) {
+                    issue_s(1, ks);
+                    mma_commit(s_full(1));
+                    mma_commit(k_empty(ks));
+                }
+            }
+            mma_commit(o_full);                               // all MMAs issued above are done
+            mbar_wait(o_full, 0, nullptr, p.status);          // drain before TMEM is released
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax (warps 0-7)
+        const int t = warp >> 2, q4 = warp & 3;
+        const int m_flat = 128 * t + 32 * q4 + lane;
+        const int hl = m_flat / p.R, rl = m_flat % p.R;
+        const int r_abs = q_row0 + rl;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * D;
+        const float sl2 = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < E; ++j) {
+            const int4 e = __ldg(&entries[j]);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, abort, p.status));
+            if (!ok) break;                          // warp-uniform: tcgen05.ld/st are collective
+            tc_fence_after();
+            uint32_t sb[kTileRows];
+#pragma unroll
+            for (int c = 0; c < kTileRows / 32; ++c)
+                tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sb[c * 32]));
+            tmem_wait_ld();
+            float s[kTileRows];
+#pragma unroll
+            for (int c = 0; c < kTileRows; ++c) s[c] = __uint_as_float(sb[c]);
+            if (e.w != 0) {
+                const int j0 = e.x * kTileRows;
+                const int hi = (e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z;
+#pragma unroll
+                for (int c = 0; c < kTileRows; ++c) {
+                    const int jj = j0 + c;
+                    if (jj < e.y || jj >= hi) s[c] = -INFINITY;
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTileRows; ++c) mx = fmaxf(mx, s[c]);
+            const float m_new = fmaxf(m_used, mx * sl2);
+            const bool need = m_new > m_used + 8.f;
+            if (j == 0) {
+                if (need) m_used = m_new;
+            } else if (__any_sync(0xffffffffu, need)) {
+                const float f = need ? ex2(m_used - m_new) : 1.f;
+                if (need) {
+                    l *= f;
+                    m_used = m_new;
+                }
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                    tmem_st32(tO + c * 32, v);
+                }
+                tmem_wait_st();
+            }
+            const float mref = m_used == -INFINITY ? 0.f : m_used;
+            float rs = 0.f;
+            uint32_t pk[kTileRows / 2];
+#pragma unroll
+            for (int c = 0; c < kTileRows / 2; ++c) {
+                const float a = ex2(fmaf(s[2 * c], sl2, -mref));
+                const float b = ex2(fmaf(s[2 * c + 1], sl2, -mref));
+                rs += a + b;
+                pk[c] = pack_bf16(a, b);
+            }
+            l += rs;
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full(t));
+        }
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
+        if (ok) {
+            tc_fence_after();
+            const bool valid = rl < n_rows;
+            const int h = g * p.G + hl;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = p.o + (static_cast<size_t>(r_abs) * p.Hq + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tO + c * 32, v);
+                tmem_wait_ld();
+                if (valid) {
+                    uint4 w[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        wp[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = w[i];
+                }
+            }
+            if (valid) p.lse[static_cast<size_t>(h) * p.N + r_abs] = (m_used + log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                         const FwdParams &p, int n_blocks, cudaStream_t stream) {
+    const int smem = FwdLayout<D>::bytes;
+    cudaError_t err = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    fwd_kernel<D><<<n_blocks * p.Hkv, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       const FwdParams &p, int n_blocks, cudaStream_t stream) {
+    if (D == 64) return launch_fwd_d<64>(tm_q, tm_k, tm_v, p, n_blocks, stream);
+    return launch_fwd_d<128>(tm_q, tm_k, tm_v, p, n_blocks, stream);
+}
+
+}  // namespace treeattn

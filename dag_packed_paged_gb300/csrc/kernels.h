@@ -1,0 +1,60 @@
+// Internal: kernel parameter blocks and launchers (implemented in the .cu files).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace treeattn {
+
+struct FwdParams {
+    const int32_t *blocks;      // 4 per query block: first row, rows, entry begin, entry end
+    const int32_t *entries;     // 4 per entry: key tile, lo, hi, flags
+    const int32_t *order;       // query blocks, longest first
+    const int32_t *page_table;  // logical page -> pool page
+    int32_t n_logical_pages;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t N;
+    int32_t Hq, Hkv, G, R;      // R = query rows per block
+    float scale_log2;           // softmax scale * log2(e)
+    __nv_bfloat16 *o;           // [N, Hq, D]
+    float *lse;                 // [Hq, N]
+    int *status;
+};
+
+struct BwdParams {
+    const int32_t *blocks;
+    const int32_t *entries;
+    const int32_t *t_entries;   // 4 per entry, key-tile-major: block, lo, hi, flags
+    const int32_t *chunks;      // 4 per chunk: tile, t_entry begin, end, partial slot
+    const int32_t *reduce;      // 4 per split tile: tile, first slot, slots, 0
+    const int32_t *order;
+    const int32_t *page_table;
+    int32_t n_logical_pages;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t N;
+    int32_t Hq, Hkv, G, R;
+    float scale;                // softmax scale
+    float scale_log2;
+    const __nv_bfloat16 *o;     // [N, Hq, D]
+    const __nv_bfloat16 *d_o;   // [N, Hq, D]
+    const float *lse;           // [Hq, N]
+    float *delta;               // [Hq, N] (workspace)
+    float *dq;                  // [N, Hq, D]
+    float *dk_pool;             // [num_pages, P, Hkv, D]
+    float *dv_pool;
+    float *partials;            // [slots, Hkv, 2, 128, D] (workspace)
+    int *status;
+};
+
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       const FwdParams &p, int n_blocks, cudaStream_t stream);
+
+cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks,
+                       int n_reduce, cudaStream_t stream);
+
+}  // namespace treeattn

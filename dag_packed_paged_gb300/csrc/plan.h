@@ -1,0 +1,69 @@
+// Internal: the plan object shared by the host planner (plan.cpp) and the launch code.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/treeattn.h"
+
+namespace treeattn {
+
+constexpr int kTileRows = 128;       // key rows per tile (the N of S = Q K^T, the K of O = P V)
+constexpr int kBlockMRows = 256;     // query (row, head) pairs per query block: two 128-lane tiles
+
+constexpr int32_t kEntryCausal = 1;  // mask key rows above the query row
+constexpr int32_t kEntryPartial = 2; // the entry covers only part of its tile
+
+void set_error(const std::string &msg);
+
+struct HostPlan {
+    ta_config cfg{};
+    int G = 1;               // query heads per KV head
+    int block_rows = 0;      // query rows per block = 256 / G
+    float scale = 0.f;
+    int64_t N = 0;
+    int64_t n_logical_pages = 0;
+
+    std::vector<int32_t> pos_ids;
+    std::vector<int32_t> blocks;      // 4 per block: first row, rows, entry begin, entry end
+    std::vector<int64_t> blk_iv_ptr;  // n_blocks + 1
+    std::vector<int32_t> iv_lo, iv_hi;
+    std::vector<int32_t> diag;        // 2 per block
+    std::vector<int32_t> entries;     // 4 per entry: tile, lo, hi, flags
+    std::vector<int32_t> t_entries;   // 4 per entry: block, lo, hi, flags (tile-major)
+    std::vector<int32_t> chunks;      // 4 per chunk: tile, t_entry begin, end, slot (-1: direct)
+    std::vector<int32_t> fwd_order;   // block ids, longest first
+    std::vector<int32_t> reduce;      // 4 per split tile: tile, first slot, slots, 0
+    std::vector<int32_t> page_table;
+    int64_t n_segments = 0;
+    int64_t n_partial_slots = 0;
+    int64_t pairs = 0;
+    double plan_ms = 0.0;
+};
+
+// Builds the host plan; returns TA_OK or an error code (message via set_error).
+int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts,
+                    int32_t n_mounts, const int32_t *page_table, int64_t n_logical_pages,
+                    const ta_config *config, HostPlan &out);
+
+}  // namespace treeattn
+
+struct ta_plan {
+    treeattn::HostPlan host;
+    // device copies (one allocation)
+    void *d_buf = nullptr;
+    size_t d_bytes = 0;
+    const int32_t *d_blocks = nullptr;
+    const int32_t *d_entries = nullptr;
+    const int32_t *d_t_entries = nullptr;
+    const int32_t *d_chunks = nullptr;
+    const int32_t *d_fwd_order = nullptr;
+    const int32_t *d_reduce = nullptr;
+    const int32_t *d_page_table = nullptr;
+    int32_t *d_status = nullptr;      // bounded-wait status words (zeroed at plan time)
+    size_t ws_delta_bytes = 0;        // workspace: delta [Hq, N] fp32, 256-aligned
+    size_t ws_bytes = 0;              // total bwd workspace
+    int device = 0;
+    int num_sms = 0;
+};

@@ -1,0 +1,233 @@
+/*
+ * treeattn -- tree/DAG-packed paged attention, forward and backward, for sm_103a (GB300).
+ *
+ * The problem (Octopus, arXiv 2611.06956, Section 3 and Section 3.3; HARTS, arXiv
+ * 2608.28158, Section 2.1 and Section 4.2): an agentic episode is a DAG of branches.  Tree
+ * edges are forks -- a child branch continues its parent after `fork_offset` rows, sharing
+ * that prefix (HARTS Section 2.2 defines the fork position as the number of shared prefix
+ * tokens).  Mount edges (Octopus Section 3.1 Table 2, read_thread; Section 3.2) lend a
+ * completed span of a sibling's rows to a reader from one of the reader's rows onwards.
+ * Every token is stored once, as one row of a compact row strip (Octopus Section 3.3 item 2:
+ * nodes concatenated topologically into one unpadded strip), and its keys/values live in a
+ * paged pool (Octopus Section 3.1 Figure 2: cursor-addressed page translation).
+ *
+ * Row r (offset i of branch b) attends exactly to its visible set vis(r): b's rows 0..i,
+ * the rows of every mount of b whose reader offset is <= i, and everything b inherited from
+ * its ancestors (the parent's rows before the fork offset, the parent's mounts active at the
+ * row before the fork, and the parent's own inheritance) -- the gather of Octopus Eq. 4
+ * [mounts || ancestors || self] with the causal triangle on the own rows (HARTS Eq. 21-22:
+ * query i sees KV entry j iff j <= h + i).  vis(r) is a set: a row reachable twice counts
+ * once.  Mounts are not transitive.
+ *
+ * All functions return 0 (TA_OK) or a negative TA_ERR_* code; tree_attn_last_error()
+ * returns a message for the calling thread's most recent failure.  No function calls
+ * exit(), abort() or traps on the GPU.
+ */
+#ifndef TREEATTN_H
+#define TREEATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TA_OK 0
+#define TA_ERR_INVALID (-1)         /* malformed DAG, page table or arguments */
+#define TA_ERR_UNSUPPORTED (-2)     /* a shape this build does not implement */
+#define TA_ERR_NOMEM (-3)           /* host or device allocation failed (planner only) */
+#define TA_ERR_CUDA (-4)            /* a CUDA runtime/driver call failed */
+#define TA_ERR_DEVICE_TIMEOUT (-5)  /* a bounded device-side wait expired; outputs are invalid */
+
+/* Flags (ta_config.flags). */
+#define TA_CLAMP_MOUNTS 0x1u  /* clamp a mount span to the source's rows instead of rejecting it
+                                 (Octopus Appendix A clamps spans to the valid range) */
+#define TA_PLAN_HOST_ONLY 0x100u /* build the plan on the host only (no device upload, no GPU
+                                    needed): for inspection with tree_attn_plan_export/_stats;
+                                    tree_attn_fwd/_bwd reject such a plan */
+
+/* A branch: `length` rows stored at compact rows [row_start, row_start + length).
+ * parent = -1 for a root (fork_offset must be 0); otherwise the child shares the parent's
+ * first `fork_offset` rows (0 <= fork_offset <= parent length). */
+typedef struct {
+    int32_t parent;
+    int32_t fork_offset;
+    int32_t length;
+    int64_t row_start;
+} ta_branch;
+
+/* A mount edge (Octopus Section 3.1 Table 2 read_thread, Section 3.2): from row
+ * `reader_offset` of branch `reader` on, the reader also sees rows [src_begin, src_end) of
+ * branch `source` (offsets within the source).  The span must be complete before the reader
+ * reads it: no mounted row may depend, through any chain of visibility, on a reader row at
+ * or after reader_offset.  A span with src_begin == src_end is ignored. */
+typedef struct {
+    int32_t reader;
+    int32_t reader_offset;
+    int32_t source;
+    int32_t src_begin;
+    int32_t src_end;
+} ta_mount;
+
+/* Attention shape.  Supported: head_dim 64 or 128; page_size 16, 32, 64 or 128;
+ * num_q_heads / num_kv_heads (query heads per KV head, consecutive grouping: query head h
+ * uses KV head h / G) in {1, 2, 4, 8, 16}.  softmax_scale <= 0 selects 1/sqrt(head_dim).
+ * num_pages is the number of pages in the K/V pools (>= the logical pages of the strip). */
+typedef struct {
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    float softmax_scale;
+    uint32_t flags;
+    int64_t num_pages;
+} ta_config;
+
+typedef struct ta_plan ta_plan; /* opaque; owned by the library */
+
+/* Counts describing a plan. */
+typedef struct {
+    int64_t n_rows;          /* N: compact rows */
+    int64_t pairs;           /* sum over rows of |vis(r)| (visible query-key row pairs) */
+    double fwd_flops;        /* useful forward FLOPs: 4 * head_dim * num_q_heads * pairs */
+    double bwd_flops;        /* useful backward FLOPs: 10 * head_dim * num_q_heads * pairs */
+    int64_t n_segments;      /* query segments (branches split at mount offsets) */
+    int64_t n_blocks;        /* query blocks */
+    int64_t n_intervals;     /* visible intervals over all blocks (diagonal excluded) */
+    int64_t n_entries;       /* (query block, key tile) work entries */
+    int64_t n_kv_tiles;      /* 128-row key tiles of the strip */
+    int64_t n_chunks;        /* dK/dV work chunks (key tile x entry range) */
+    int64_t n_partial_slots; /* dK/dV partial accumulators for split key tiles */
+    int32_t block_rows;      /* query rows per block (256 / G) */
+    int32_t tile_rows;       /* key rows per tile (128) */
+    size_t bwd_workspace_bytes;
+    double plan_ms;          /* host time spent in tree_attn_plan */
+} ta_plan_stats;
+
+/* Host views of the plan's arrays, for inspection and bit-exact tests.  All pointers are
+ * owned by the plan and stay valid until tree_attn_plan_destroy.
+ *   pos_ids[n_rows]                    Eq. 2 position of every compact row
+ *   blocks[4*n_blocks]                 {first row, rows, first entry, end entry}
+ *   blk_iv_ptr[n_blocks+1], iv_lo/iv_hi[n_intervals]
+ *                                      per block: sorted disjoint maximal intervals of rows
+ *                                      visible to every row of the block
+ *   diag[2*n_blocks]                   per block: own rows [lo, hi) seen causally (j <= r)
+ *   entries[4*n_entries]               query-major {key tile, lo, hi, flags}
+ *   t_entries[4*n_entries]             key-tile-major {block, lo, hi, flags}
+ *   chunks[4*n_chunks]                 {key tile, first t_entry, end t_entry, partial slot or -1}
+ *   fwd_order[n_blocks]                order in which query blocks are launched
+ * flags: bit 0 = causal (mask j > r), bit 1 = the entry does not cover its whole tile. */
+typedef struct {
+    int64_t n_rows, n_blocks, n_intervals, n_entries, n_chunks;
+    const int32_t *pos_ids;
+    const int32_t *blocks;
+    const int64_t *blk_iv_ptr;
+    const int32_t *iv_lo, *iv_hi;
+    const int32_t *diag;
+    const int32_t *entries;
+    const int32_t *t_entries;
+    const int32_t *chunks;
+    const int32_t *fwd_order;
+} ta_plan_arrays;
+
+/*
+ * tree_attn_plan -- validate an episode DAG and build the work plan (host C++).
+ *
+ * Splits branches into query segments at mount offsets (Octopus Section 3.3 item 1, node
+ * splitting at read_thread boundaries; forks do not change a branch's own rows), computes
+ * Eq. 2 position ids (Octopus Section 3.2), tiles each segment into query blocks, lists
+ * per block the visible key-row intervals (Eq. 4 gather, expressed as row intervals rather
+ * than copied), translates them into 128-row key tiles, builds the key-tile-major transpose
+ * used by the dK/dV reduction, and uploads everything to the device on `stream`
+ * (synchronising once).
+ *
+ *   branches[n_branches], mounts[n_mounts]   host arrays, read during the call only
+ *   page_table[n_logical_pages]             host: logical page l of the strip (rows
+ *                                           [l*page_size, (l+1)*page_size)) is pool page
+ *                                           page_table[l]; entries distinct, < num_pages;
+ *                                           n_logical_pages >= ceil(N / page_size)
+ *   config                                  attention shape (see ta_config)
+ *   pos_ids_out                             host int32[N] or NULL: receives the positions
+ *   stream                                  cudaStream_t (may be NULL: the default stream)
+ *   out                                     receives the plan; *out is NULL on failure
+ *
+ * Errors: TA_ERR_INVALID for a bad parent or a parent cycle, a root with a fork offset, a
+ * fork offset beyond its parent, negative lengths, branch row ranges that overlap or leave
+ * gaps in [0, N), N beyond 2^31-1, a mount with an index or offset out of range or a span
+ * outside its source (unless TA_CLAMP_MOUNTS), a non-causal mount, a short page table, a
+ * duplicate or out-of-range page; TA_ERR_UNSUPPORTED for shapes outside ta_config's list;
+ * TA_ERR_NOMEM, TA_ERR_CUDA.  An empty DAG (N = 0) gives a valid plan on which fwd and
+ * bwd do nothing.
+ */
+int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts,
+                   int32_t n_mounts, const int32_t *page_table, int64_t n_logical_pages,
+                   const ta_config *config, int32_t *pos_ids_out, void *stream, ta_plan **out);
+
+/*
+ * tree_attn_fwd -- O and logsumexp of every compact row (device, sm_103a).
+ *
+ *   O[r,h]   = sum_{j in vis(r)} softmax_j(scale <q[r,h], k[j,g]>) v[j,g],  g = h / G
+ *   lse[h,r] = ln sum_{j in vis(r)} exp(scale <q[r,h], k[j,g]>)
+ * (Octopus Section 3.3 Eq. 4 and the rectangular causal attention that follows it; HARTS
+ * Section 4.2 Eq. 21-22.)
+ *
+ *   q       device bf16 [N, Hq, D], compact rows, contiguous; 16-byte aligned
+ *   k_pool  device bf16 [num_pages, page_size, Hkv, D]; 16-byte aligned.  Rows of the last
+ *   v_pool  logical page at or beyond N are read as part of whole tiles and must be finite
+ *           (pages not listed in the page table are never read)
+ *   o       device bf16 [N, Hq, D] (written)
+ *   lse     device fp32 [Hq, N] (written), natural log
+ * Everything is enqueued on `stream`; no allocation, no synchronisation.  Caller owns every
+ * buffer.  Returns TA_ERR_INVALID for NULL/misaligned pointers, TA_ERR_CUDA for a launch
+ * failure, TA_ERR_DEVICE_TIMEOUT if an earlier launch on this plan reported an expired
+ * bounded wait (the status is read back only by tree_attn_check).
+ */
+int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
+                  void *o, float *lse, void *stream);
+
+/*
+ * tree_attn_bwd -- gradients of sum <dO, O> w.r.t. q, k_pool and v_pool (device, sm_103a).
+ *
+ *   delta[h,r] = <dO[r,h], O[r,h]>
+ *   dS         = P * (<dO[r,h], v[j,g]> - delta),  P recomputed from lse
+ *   dq[r,h]    = scale sum_{j in vis(r)} dS k[j,g]
+ *   dk[j,g]    = scale sum over every (r, h in g) with j in vis(r) of dS q[r,h]
+ *   dv[j,g]    = sum over the same readers of P dO[r,h]
+ * Gradients of a shared prefix row or a mounted row are summed over all of its readers --
+ * tree descendants and mount readers -- and written exactly once (Octopus Section 3.4,
+ * differentiable mount edges; HARTS Section 3.4, gather backward accumulates every consumer
+ * into the unique compact row).
+ *
+ *   q, k_pool, v_pool, o, lse   as in tree_attn_fwd (o, lse: that call's outputs)
+ *   d_o     device bf16 [N, Hq, D]: upstream gradient per compact row (a caller with several
+ *           semantic positions per row sums their gradients first)
+ *   dq      device fp32 [N, Hq, D] (written)
+ *   dk_pool device fp32 [num_pages, page_size, Hkv, D]: rows of the strip's logical pages are
+ *   dv_pool written; other pages are left untouched
+ *   workspace, ws_bytes   device scratch of at least tree_attn_bwd_workspace_size(plan)
+ *           bytes, 256-byte aligned, owned by the caller; contents need not be initialised
+ * Returns as tree_attn_fwd, plus TA_ERR_INVALID for a short workspace.
+ */
+int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
+                  const void *o, const float *lse, const void *d_o, float *dq, float *dk_pool,
+                  float *dv_pool, void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of device scratch tree_attn_bwd needs for this plan (delta and dK/dV partials). */
+size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
+
+/* Synchronises `stream` and reports whether any bounded device wait of this plan's kernels
+ * expired since the last check (TA_ERR_DEVICE_TIMEOUT) or a CUDA error is pending
+ * (TA_ERR_CUDA); clears the status. */
+int tree_attn_check(const ta_plan *plan, void *stream);
+
+int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out);
+int tree_attn_plan_export(const ta_plan *plan, ta_plan_arrays *out);
+void tree_attn_plan_destroy(ta_plan *plan);
+const char *tree_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEATTN_H */

@@ -1,0 +1,262 @@
+"""Planner tests (CPU): the plan's positions, visible intervals, key-tile entries and
+transpose are compared bit-exactly with the oracle's explicit enumeration from the DAG."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import dag
+import dag_packed_paged_gb300 as ta
+from dag_packed_paged_gb300 import workloads as W
+
+T = 128
+
+
+def host_plan(ep, mounts=None, page_table=None, flags=0, **over):
+    mounts = ep.mounts if mounts is None else mounts
+    n_logical = -(-ep.n_rows // ep.page_size)
+    pt = np.arange(n_logical, dtype=np.int32) if page_table is None else page_table
+    kw = dict(num_q_heads=ep.num_q_heads, num_kv_heads=ep.num_kv_heads, head_dim=ep.head_dim,
+              page_size=ep.page_size, num_pages=max(n_logical, 1) + 3)
+    kw.update(over)
+    return ta.tree_attn_plan(ep.branches, mounts, pt, flags=flags | ta.TA_PLAN_HOST_ONLY, **kw)
+
+
+def _merge(iv):
+    out = []
+    for a, z in sorted(iv):
+        if out and a <= out[-1][1]:
+            out[-1] = (out[-1][0], max(out[-1][1], z))
+        else:
+            out.append((a, z))
+    return out
+
+
+def _intervals_to_set_runs(lo, hi):
+    return [(int(a), int(b)) for a, b in zip(lo, hi)]
+
+
+def check_plan_against_oracle(ep, rows_to_check=None):
+    plan = host_plan(ep)
+    ex = ta.tree_attn_plan_export(plan)
+    st = ta.tree_attn_plan_stats(plan)
+    N = ep.n_rows
+    # positions (Eq. 2): bit-exact
+    assert (ex["pos_ids"] == dag.positions(ep.branches, ep.mounts)).all()
+    assert (plan.pos_ids == ex["pos_ids"]).all()
+    # visible sets: per row, block intervals + own rows [diag_lo, r] == oracle enumeration
+    rows, ptr, olo, ohi = dag.visible_intervals(ep.branches, ep.mounts)
+    blocks, diag, ivp = ex["blocks"], ex["diag"], ex["blk_iv_ptr"]
+    covered = np.zeros(N, dtype=np.int64)
+    check = set(range(N)) if rows_to_check is None else set(rows_to_check)
+    for b in range(len(blocks)):
+        r0, n, e0, e1 = (int(x) for x in blocks[b])
+        assert diag[b, 0] == r0 and diag[b, 1] == r0 + n and n <= plan_block_rows(ep)
+        ivs = _intervals_to_set_runs(ex["iv_lo"][ivp[b]:ivp[b + 1]], ex["iv_hi"][ivp[b]:ivp[b + 1]])
+        # sorted, disjoint, maximal, none touching the diagonal from above
+        for (a, z), (a2, z2) in zip(ivs, ivs[1:]):
+            assert a < z < a2 < z2
+        ents = ex["entries"][e0:e1]
+        for r in range(r0, r0 + n):
+            covered[r] += 1
+            if r not in check:
+                continue
+            want = _intervals_to_set_runs(olo[ptr[r]:ptr[r + 1]], ohi[ptr[r]:ptr[r + 1]])
+            got = _merge(ivs + [(r0, r + 1)])
+            assert got == want, (r, got, want)
+            # the key-tile entries cover exactly the same rows, once each
+            mark = np.zeros(N, dtype=np.int32)
+            for tile, lo, hi, fl in ents:
+                assert tile * T <= lo < hi <= (tile + 1) * T
+                assert bool(fl & 2) == (lo != tile * T or hi != (tile + 1) * T)
+                top = min(hi, r + 1) if fl & 1 else hi
+                mark[lo:max(lo, top)] += 1
+            wmask = np.zeros(N, dtype=np.int32)
+            for a, z in want:
+                wmask[a:z] = 1
+            assert (mark == wmask).all(), r
+    assert (covered == 1).all()
+    # causal flag only where some key lies above the block's first row
+    for b in range(len(blocks)):
+        r0, n, e0, e1 = (int(x) for x in blocks[b])
+        for tile, lo, hi, fl in ex["entries"][e0:e1]:
+            if fl & 1:
+                assert hi - 1 > r0
+    # transpose: same entries grouped by key tile; chunks cover every tile's range once
+    ents, te = ex["entries"], ex["t_entries"]
+    assert len(ents) == len(te) == st["n_entries"]
+    fwd = sorted((int(b), int(lo), int(hi), int(fl)) for b in range(len(blocks))
+                 for (_, lo, hi, fl) in ents[blocks[b, 2]:blocks[b, 3]])
+    assert sorted(map(tuple, te.tolist())) == fwd
+    tiles_of_te = np.empty(len(te), dtype=np.int64)
+    for i, (b, lo, hi, fl) in enumerate(te):
+        tiles_of_te[i] = lo // T
+    assert (np.diff(tiles_of_te) >= 0).all()
+    seen = np.zeros(len(te), dtype=np.int32)
+    slots = []
+    for tile, a, z, slot in ex["chunks"]:
+        assert (tiles_of_te[a:z] == tile).all() and z > a
+        seen[a:z] += 1
+        if slot >= 0:
+            slots.append(int(slot))
+    assert (seen == 1).all()
+    assert sorted(slots) == list(range(len(slots))) and len(slots) == st["n_partial_slots"]
+    assert sorted(ex["fwd_order"].tolist()) == list(range(len(blocks)))
+    # pair count
+    assert st["pairs"] == int((ohi - olo).sum()) == dag.count_pairs(ep.branches, ep.mounts)
+    assert st["n_rows"] == N
+    return plan, ex, st
+
+
+def plan_block_rows(ep):
+    return 256 // (ep.num_q_heads // ep.num_kv_heads)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_full_configs(cfg):
+    ep = W.config(cfg)
+    rng = np.random.default_rng(cfg)
+    rows = None if ep.n_rows < 50_000 else rng.choice(ep.n_rows, 3000, replace=False)
+    check_plan_against_oracle(ep, rows)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_small(seed):
+    ep = W.random_small(seed, max_branches=8, max_len=300, n_mounts=int(seed % 4))
+    check_plan_against_oracle(ep)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_gqa_shapes(seed):
+    heads = [(1, 1), (2, 1), (8, 1), (16, 1), (16, 2), (32, 8)][seed]
+    ep = W.random_small(100 + seed, max_branches=6, max_len=400, heads=heads, head_dim=128,
+                        page_size=[16, 32, 64, 128][seed % 4])
+    check_plan_against_oracle(ep)
+
+
+def test_crafted():
+    from test_oracle_pins import crafted
+    check_plan_against_oracle(crafted())
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_zero_length_mounts_give_identical_plan(seed):
+    ep = W.random_small(seed, max_len=200)
+    rng = np.random.default_rng(seed)
+    rows = [tuple(int(x) for x in m) for m in ep.mounts]
+    for _ in range(5):
+        r = int(rng.integers(0, len(ep.branches)))
+        s = int(rng.integers(0, len(ep.branches)))
+        b = int(rng.integers(0, int(ep.branches["length"][s]) + 1))
+        rows.append((r, int(rng.integers(0, int(ep.branches["length"][r]))), s, b, b))
+    rng.shuffle(rows)
+    a = ta.tree_attn_plan_export(host_plan(ep))
+    b = ta.tree_attn_plan_export(host_plan(ep, mounts=W.make_mounts(rows)))
+    for k in a:
+        assert np.array_equal(np.asarray(a[k]), np.asarray(b[k])), k
+
+
+def test_planner_matches_eq2_example():
+    # the worked example after Octopus Eq. 2, through the library planner
+    br = W.make_branches([-1, 0, 0], [0, 1500, 1500], [1500, 2501, 505])
+    mt = W.make_mounts([(2, 500, 1, 0, 2501)])
+    ep = W.Episode("eq2", br, mt, 4, 1, 64, 16)
+    ex = ta.tree_attn_plan_export(host_plan(ep))
+    b0 = int(br["row_start"][2])
+    assert ex["pos_ids"][b0 + 499] == 1999 and ex["pos_ids"][b0 + 500] == 4001
+
+
+def test_empty_dag():
+    ep = W.Episode("empty", W.make_branches([], [], []), W.make_mounts([]), 4, 1, 64, 16)
+    plan = host_plan(ep, page_table=np.zeros(0, np.int32))
+    st = ta.tree_attn_plan_stats(plan)
+    assert st["n_rows"] == 0 and st["n_blocks"] == 0 and st["pairs"] == 0
+
+
+def _expect(code, ep, **kw):
+    with pytest.raises(ta.TreeAttnError) as ei:
+        host_plan(ep, **kw)
+    assert ei.value.code == code, str(ei.value)
+
+
+def _raw_branches(parents, forks, lens, starts=None):
+    br = np.zeros(len(parents), dtype=W.BRANCH_DTYPE)
+    br["parent"], br["fork_offset"], br["length"] = parents, forks, lens
+    br["row_start"] = np.concatenate([[0], np.cumsum(lens)[:-1]]) if starts is None else starts
+    return br
+
+
+def test_rejects_invalid_dags():
+    mk = _raw_branches
+    base = W.tiny()
+    E = lambda br, mt=None: W.Episode("x", br, W.make_mounts(mt or []), 4, 1, 64, 16)
+    _expect(ta.TA_ERR_INVALID, E(mk([-1, 5], [0, 1], [10, 10])))                  # bad parent
+    _expect(ta.TA_ERR_INVALID, E(mk([-1, 0], [0, 11], [10, 10])))                 # fork > parent length
+    _expect(ta.TA_ERR_INVALID, E(mk([-1], [3], [10])))                            # root with a fork offset
+    br = mk([1, 0], [4, 4], [10, 10])                                            # parent cycle
+    _expect(ta.TA_ERR_INVALID, E(br))
+    br = mk([-1, 0], [0, 4], [10, 10]); br["row_start"][1] = 8                     # overlapping rows
+    _expect(ta.TA_ERR_INVALID, E(br))
+    br = mk([-1, 0], [0, 4], [10, 10]); br["row_start"][1] = 12                    # gap
+    _expect(ta.TA_ERR_INVALID, E(br))
+    br = mk([-1, 0, 0], [0, 4, 4], [10, 10, 10])
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 2, 2, 0, 11)]))                         # span beyond source
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 10, 2, 0, 3)]))                         # offset beyond reader
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 2, 7, 0, 3)]))                          # bad source index
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 2, 1, 0, 5)]))                          # reads its own future
+    br = mk([-1, 0, 1], [0, 4, 6], [10, 10, 10])
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 3, 2, 0, 2)]))                          # reads a descendant forked after the mount
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 3, 2, 0, 2)]))
+    br = mk([-1, 0, 0], [0, 4, 4], [10, 10, 10])
+    _expect(ta.TA_ERR_INVALID, E(br, [(1, 3, 2, 0, 5), (2, 2, 1, 0, 5)]))         # mutual mounts
+    # a mount that only becomes non-causal through another mount (transitively)
+    br = mk([-1, 0, 0, 0], [0, 4, 4, 4], [10, 10, 10, 10])
+    _expect(ta.TA_ERR_INVALID, E(br, [(2, 1, 1, 0, 9), (3, 1, 2, 0, 5), (1, 2, 3, 0, 4)]))
+    # short page table, duplicate page, page out of range
+    n_log = -(-base.n_rows // base.page_size)
+    _expect(ta.TA_ERR_INVALID, base, page_table=np.arange(n_log - 1, dtype=np.int32))
+    pt = np.arange(n_log, dtype=np.int32); pt[3] = pt[4]
+    _expect(ta.TA_ERR_INVALID, base, page_table=pt)
+    pt = np.arange(n_log, dtype=np.int32); pt[3] = 10_000
+    _expect(ta.TA_ERR_INVALID, base, page_table=pt)
+
+
+def test_valid_edge_mounts_accepted():
+    mk = W.make_branches
+    E = lambda br, mt=None: W.Episode("x", br, W.make_mounts(mt or []), 4, 1, 64, 16)
+    br = mk([-1, 0, 1], [0, 4, 6], [10, 10, 10])
+    host_plan(E(br, [(1, 7, 2, 0, 2)]))            # reads a descendant forked before the mount
+    host_plan(E(br, [(1, 5, 1, 0, 5)]))            # reads its own completed past
+    br = mk([-1, 0, 0], [0, 10, 10], [10, 10, 10])
+    host_plan(E(br, [(1, 3, 2, 0, 5), (2, 6, 1, 0, 3)]))  # mutual, but each span is complete
+
+
+def test_clamp_flag():
+    mk = W.make_branches
+    br = mk([-1, 0, 0], [0, 4, 4], [10, 10, 10])
+    ep = W.Episode("x", br, W.make_mounts([(1, 2, 2, 5, 40)]), 4, 1, 64, 16)
+    _expect(ta.TA_ERR_INVALID, ep)
+    a = ta.tree_attn_plan_export(host_plan(ep, flags=ta.TA_CLAMP_MOUNTS))
+    ep2 = W.Episode("x", br, W.make_mounts([(1, 2, 2, 5, 10)]), 4, 1, 64, 16)
+    b = ta.tree_attn_plan_export(host_plan(ep2))
+    for k in a:
+        assert np.array_equal(np.asarray(a[k]), np.asarray(b[k])), k
+    ep3 = W.Episode("x", br, W.make_mounts([(1, 2, 2, 20, 40)]), 4, 1, 64, 16)   # emptied by the clamp
+    c = ta.tree_attn_plan_export(host_plan(ep3, flags=ta.TA_CLAMP_MOUNTS))
+    d = ta.tree_attn_plan_export(host_plan(W.Episode("x", br, W.make_mounts([]), 4, 1, 64, 16)))
+    for k in c:
+        assert np.array_equal(np.asarray(c[k]), np.asarray(d[k])), k
+
+
+def test_rejects_unsupported_shapes():
+    ep = W.tiny()
+    _expect(ta.TA_ERR_UNSUPPORTED, ep, head_dim=96)
+    _expect(ta.TA_ERR_UNSUPPORTED, ep, page_size=8)
+    _expect(ta.TA_ERR_UNSUPPORTED, ep, num_q_heads=6, num_kv_heads=4)
+    _expect(ta.TA_ERR_UNSUPPORTED, ep, num_q_heads=96, num_kv_heads=3)
+
+
+def test_fwd_rejects_host_only_plan():
+    plan = host_plan(W.tiny())
+    with pytest.raises(ta.TreeAttnError) as ei:
+        ta.tree_attn_fwd(plan, 16, 16, 16, 16, 16, stream=0)
+    assert ei.value.code == ta.TA_ERR_INVALID
