@@ -1,0 +1,423 @@
+"""Benchmark: tree/DAG-packed attention forward + backward on GB300.
+
+One step = one pass of the whole hot path over one synthetic episode batch: the forward
+(O, lse) and the backward (delta, dQ, dK/dV, reduction), through the C ABI, with the plan
+built once (it is reused by every layer with the same topology; planning time is reported
+separately and included in the end-to-end figure).  Default workload: the mount-heavy DAG
+(4 independent DAGs of 65,536 rows; a 4,096-row producer span mounted by 32 readers each;
+GQA 16/4, head_dim 128, page 64; bf16 inputs ~ N(0,1)/sqrt(128)).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own episode batch of the same shape on its own GPU
+(weak scaling, no data-path collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dag_packed_paged_gb300 import workloads as W  # noqa: E402
+
+METRIC = "tree-packed attention fwd & fwd+bwd useful TFLOP/s, % of GB300 BF16 peak"
+WORKLOADS = {
+    "tiny_tree": 0, "balanced_tree": 1, "commander_worker_dag": 2, "irregular_tree": 3,
+    "mount_heavy": 4,
+}
+DESCRIPTION = {
+    0: "tiny tree: 256-row root, 3 x 128-row branches, 1 mount; GQA 4/1, D=64, page 16",
+    1: "balanced rollout tree: 4096-row root, fan-out 4 at depth 1 and 2, 2048-row edges; GQA 16/4, D=128, page 64",
+    2: "commander-worker DAG: 8192-row root, 8 workers of U[8192,32768] rows, 12 mounts of 1-4 pages; GQA 16/4, D=128, page 64",
+    3: "irregular rollout tree: 64 trajectories, lognormal(7,1) edges, unaligned forks, expanded/compact 6.05; GQA 32/8, D=128, page 64",
+    4: "mount-heavy: 4 DAGs x 65,536 rows, 4096-row producer span mounted by 32 readers each; GQA 16/4, D=128, page 64",
+}
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = {"dkdv": "bwd.cu", "dq": "bwd.cu", "fwd": "fwd.cu"}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash(kernel):
+    src = os.path.join(ROOT, "dag_packed_paged_gb300", "csrc", KERNEL_SOURCES[kernel])
+    h = hashlib.sha256()
+    for f in (src, os.path.join(ROOT, "dag_packed_paged_gb300", "csrc", "ptx.cuh")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of that kernel (the summary records the source hash); otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            if parts[2] == kernel_hash(kernel):
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_uuid=None):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.uuid = dev_uuid
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.uuid:
+                cmd.insert(1, f"--id={self.uuid}")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        load = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank number over all ranks (the step time of a weak-scaling job)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Every rank runs its own episode batch of the same shape."""
+    return seed + rank
+
+
+def bf16_dev(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def cpu_baseline(ep, t, target_s=15.0, seed=0):
+    """The fp64 CPU oracle, as it stands, on a bounded sample of query rows of the same
+    workload: forward, dQ and the rows' dK/dV contributions.  Useful FLOPs are counted with
+    the same convention as the GPU (14 * D * Hq * visible pairs of the sampled rows)."""
+    import oracle
+    from oracle import dag
+    rng = np.random.default_rng(seed)
+    N = ep.n_rows
+
+    def run(rows):
+        iv = dag.visible_intervals(ep.branches, ep.mounts, rows)
+        t0 = time.perf_counter()
+        f = oracle.forward(ep.branches, ep.mounts, t.q, t.k, t.v, ep.softmax_scale, intervals=iv)
+        b = oracle.backward(ep.branches, ep.mounts, t.q, t.k, t.v, t.do, ep.softmax_scale, f)
+        dt = time.perf_counter() - t0
+        pairs = int((iv[3] - iv[2]).sum())
+        return dt, pairs, b.threads
+
+    probe = rng.choice(N, 8, replace=False)
+    dt, pairs, _ = run(probe)
+    n = int(min(4096, max(16, 8 * target_s / max(dt, 1e-3))))
+    rows = rng.choice(N, n, replace=False)
+    dt, pairs, threads = run(rows)
+    flops = 14.0 * ep.head_dim * ep.num_q_heads * pairs
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"{n} seeded random query rows of the same workload ({pairs} visible pairs): fp64 forward, "
+                      f"dQ and their dK/dV contributions, on {threads} host threads"}
+
+
+def run_reference(args, ep, world, rank):
+    """The reference arm: the CPU oracle, timed as it stands on bounded samples."""
+    if rank != 0:
+        return
+    t = W.make_tensors(ep)
+    import oracle
+    from oracle import dag
+    rng = np.random.default_rng(123)
+    oracle.build()
+    rows_per_step = 48
+    total_pairs, total_s, threads = 0, 0.0, 0
+    for step in range(args.warmup + args.steps):
+        rows = rng.choice(ep.n_rows, rows_per_step, replace=False)
+        iv = dag.visible_intervals(ep.branches, ep.mounts, rows)
+        t0 = time.perf_counter()
+        f = oracle.forward(ep.branches, ep.mounts, t.q, t.k, t.v, ep.softmax_scale, intervals=iv)
+        b = oracle.backward(ep.branches, ep.mounts, t.q, t.k, t.v, t.do, ep.softmax_scale, f)
+        dt = time.perf_counter() - t0
+        threads = b.threads
+        if step >= args.warmup:
+            total_s += dt
+            total_pairs += int((iv[3] - iv[2]).sum())
+    flops = 14.0 * ep.head_dim * ep.num_q_heads * total_pairs
+    value = flops / total_s / 1e12
+    sample = f"{rows_per_step} seeded random query rows per step: fp64 forward, dQ and their dK/dV contributions"
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(ep, args), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(ep, args, stats=None):
+    cfg = {"workload": DESCRIPTION[WORKLOADS[args.workload]], "name": args.workload, "rows": ep.n_rows,
+           "branches": int(len(ep.branches)), "mounts": int(len(ep.mounts)),
+           "heads_q": ep.num_q_heads, "heads_kv": ep.num_kv_heads, "head_dim": ep.head_dim,
+           "page_size": ep.page_size, "seed": ep.seed}
+    in_bytes = ep.n_rows * (2 * ep.num_q_heads + 2 * ep.num_kv_heads) * ep.head_dim * 2
+    cfg["l2"] = (f"inputs ({in_bytes / 1e9:.2f} GB of Q, K, V, dO) larger than the 129 MB L2; no flush between steps"
+                 if in_bytes > 129e6 else f"inputs ({in_bytes / 1e6:.1f} MB) fit in L2: not a timing workload")
+    if stats:
+        cfg["pairs"] = int(stats["pairs"])
+        cfg["fwd_useful_tflop"] = stats["fwd_flops"] / 1e12
+        cfg["fwdbwd_useful_tflop"] = (stats["fwd_flops"] + stats["bwd_flops"]) / 1e12
+    return cfg
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="mount_heavy", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    ep = W.config(WORKLOADS[args.workload])
+
+    if args.impl == "reference":
+        run_reference(args, ep, world, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import dag_packed_paged_gb300 as ta
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    ep.seed = rank_seed(ep.seed, rank)
+    t = W.make_tensors(ep)
+    pool = W.make_pool(ep, t)
+    N, Hq, Hkv, D = ep.n_rows, ep.num_q_heads, ep.num_kv_heads, ep.head_dim
+
+    def plan_now():
+        return ta.tree_attn_plan(ep.branches, ep.mounts, pool.page_table, num_q_heads=Hq, num_kv_heads=Hkv,
+                                 head_dim=D, page_size=ep.page_size, num_pages=pool.k_pool.shape[0])
+
+    plan_times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        plan = plan_now()
+        plan_times.append(1000 * (time.perf_counter() - t0))
+    st = ta.tree_attn_plan_stats(plan)
+    q = bf16_dev(t.q, dev)
+    k_pool = bf16_dev(pool.k_pool, dev)
+    v_pool = bf16_dev(pool.v_pool, dev)
+    d_o = bf16_dev(t.do, dev)
+    o = torch.empty((N, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, N), dtype=torch.float32, device=dev)
+    dq = torch.empty((N, Hq, D), dtype=torch.float32, device=dev)
+    dk_pool = torch.zeros(pool.k_pool.shape, dtype=torch.float32, device=dev)
+    dv_pool = torch.zeros(pool.v_pool.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(ta.tree_attn_bwd_workspace_size(plan), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ta.tree_attn_fwd(plan, q, k_pool, v_pool, o, lse)
+        ta.tree_attn_bwd(plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, ws)
+
+    for _ in range(args.warmup):
+        step()
+    ta.tree_attn_check(plan)
+
+    # ---------------------------------------------------------------- timed region
+    K = args.steps
+    trace = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for evs in trace:                          # torch creates the CUDA event on first record
+        for e in evs:
+            e.record(stream)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid if rank == 0 else None) as clocks:
+        time.sleep(0.3)
+        ev0.record(stream)
+        for k in range(K):
+            ta.tree_attn_set_trace_events(plan, trace[k])
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        time.sleep(0.2)
+    ta.tree_attn_set_trace_events(plan, None)
+    if world > 1:
+        dist.barrier()
+    ta.tree_attn_check(plan)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, dev)
+
+    def avg(a, b):
+        return sum(trace[k][a].elapsed_time(trace[k][b]) for k in range(K)) / K
+
+    n_reduce = st["n_partial_slots"] > 0
+    kern_ms = {"fwd": avg(0, 1), "delta": avg(2, 3), "dq": avg(3, 4), "dkdv": avg(4, 5), "reduce": avg(5, 6)}
+    flops_fwd, flops_bwd = st["fwd_flops"], st["bwd_flops"]
+    base = ep.head_dim * ep.num_q_heads * st["pairs"]
+    algo = {"fwd": 4 * base, "dq": 6 * base, "dkdv": 8 * base}
+    dominant = max(("fwd", "dq", "dkdv"), key=lambda k: kern_ms[k])
+    peaks, peak_kind = load_peaks()
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    achieved = algo[dominant] / kern_ms[dominant] / 1e9
+    traffic = recorded_traffic(dominant, args.workload)
+    value = (flops_fwd + flops_bwd) * world / ms / 1e9
+    fwd_tflops = flops_fwd / kern_ms["fwd"] / 1e9
+
+    # ---------------------------------------------------------------- end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_q = torch.from_numpy(t.q.view(np.int16)).pin_memory()
+        h_k = torch.from_numpy(pool.k_pool.view(np.int16)).pin_memory()
+        h_v = torch.from_numpy(pool.v_pool.view(np.int16)).pin_memory()
+        h_do = torch.from_numpy(t.do.view(np.int16)).pin_memory()
+        outs = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()),
+                (lse, torch.empty(lse.shape, dtype=lse.dtype).pin_memory()),
+                (dq, torch.empty(dq.shape, dtype=dq.dtype).pin_memory()),
+                (dk_pool, torch.empty(dk_pool.shape, dtype=dk_pool.dtype).pin_memory()),
+                (dv_pool, torch.empty(dv_pool.shape, dtype=dv_pool.dtype).pin_memory())]
+        ins = [(q, h_q), (k_pool, h_k), (v_pool, h_v), (d_o, h_do)]
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        d2h = sum(h.numel() * h.element_size() for _, h in outs)
+        e2e_steps = max(2, min(K, 5))
+
+        def e2e_step():
+            p2 = plan_now()                                   # host planner + plan upload
+            for dv_, hv in ins:
+                dv_.view(torch.int16).copy_(hv, non_blocking=True)
+            ta.tree_attn_fwd(p2, q, k_pool, v_pool, o, lse)
+            ta.tree_attn_bwd(p2, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, ws)
+            for dv_, hv in outs:
+                hv.copy_(dv_, non_blocking=True)
+            return p2
+
+        keep = e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            keep = e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        del keep
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+        e2e = {"value": (flops_fwd + flops_bwd) * world / e2e_ms / 1e9, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+               "steps": e2e_steps, "includes": "plan + H2D of q/k_pool/v_pool/dO from pinned host + fwd + bwd "
+                                               "+ D2H of o/lse/dq/dk_pool/dv_pool"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(ep, args, st),
+        "fwd_tflops": fwd_tflops,
+        "fwd_frac_of_peak": fwd_tflops / burst, "fwdbwd_frac_of_peak": value / world / burst,
+        "peak_tflops": {"burst": burst, "sustained": sustained, "kind": peak_kind},
+        "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()},
+        "plan_ms": statistics.median(plan_times),
+        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": sustained,
+                     "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": traffic,
+                     "peak_kind": f"bf16 dense, sustained ({peak_kind})",
+                     "algorithmic": f"{algo[dominant] / 1e12:.3f} TFLOP per launch ({2 * {'fwd': 2, 'dq': 3, 'dkdv': 4}[dominant]}*D*Hq*pairs)"},
+        "gpu_launches": K * (1 + 3 + (1 if n_reduce else 0)),
+        "e2e": e2e,
+    }
+    if rank == 0:
+        line["clocks"] = clocks.summary()
+        if world == 1 and not args.no_cpu_baseline:
+            try:
+                line["cpu_baseline"] = cpu_baseline(ep, t)
+            except Exception as ex:  # report, do not hide, a failed baseline
+                line["cpu_baseline"] = {"error": str(ex)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

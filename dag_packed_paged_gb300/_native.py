@@ -108,6 +108,8 @@ def lib():
     L.tree_attn_plan_export.restype = ctypes.c_int
     L.tree_attn_plan_destroy.argtypes = [vp]
     L.tree_attn_plan_destroy.restype = None
+    L.tree_attn_set_trace_events.argtypes = [vp, ctypes.POINTER(vp), ctypes.c_int]
+    L.tree_attn_set_trace_events.restype = ctypes.c_int
     L.tree_attn_last_error.argtypes = []
     L.tree_attn_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -203,6 +205,16 @@ def tree_attn_bwd_workspace_size(plan: Plan) -> int:
 
 def tree_attn_check(plan: Plan, stream=None) -> None:
     _check(lib().tree_attn_check(plan.handle, _stream(stream)))
+
+
+def tree_attn_set_trace_events(plan: Plan, events) -> None:
+    """events: None, or 7 torch.cuda.Event objects (or None entries) -- see the header."""
+    if events is None:
+        _check(lib().tree_attn_set_trace_events(plan.handle, None, 0))
+        return
+    arr = (ctypes.c_void_p * 7)(*[None if e is None else e.cuda_event for e in events])
+    plan._trace_keepalive = events
+    _check(lib().tree_attn_set_trace_events(plan.handle, arr, 7))
 
 
 def tree_attn_plan_stats(plan: Plan) -> dict:

@@ -133,11 +133,12 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         size_t bytes;
         size_t off;
     };
-    Part parts[8] = {
+    Part parts[10] = {
         {h.blocks.data(), h.blocks.size() * 4, 0},   {h.entries.data(), h.entries.size() * 4, 0},
         {h.t_entries.data(), h.t_entries.size() * 4, 0}, {h.chunks.data(), h.chunks.size() * 4, 0},
         {h.fwd_order.data(), h.fwd_order.size() * 4, 0}, {h.reduce.data(), h.reduce.size() * 4, 0},
         {h.page_table.data(), h.page_table.size() * 4, 0}, {nullptr, 64, 0},
+        {h.tile_rows.data(), h.tile_rows.size() * 4, 0}, {h.t_info.data(), h.t_info.size() * 4, 0},
     };
     size_t total = 0;
     for (Part &p : parts) {
@@ -174,6 +175,8 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     plan->d_reduce = reinterpret_cast<const int32_t *>(d + parts[5].off);
     plan->d_page_table = reinterpret_cast<const int32_t *>(d + parts[6].off);
     plan->d_status = reinterpret_cast<int32_t *>(d + parts[7].off);
+    plan->d_tile_rows = reinterpret_cast<const int32_t *>(d + parts[8].off);
+    plan->d_t_info = reinterpret_cast<const int32_t *>(d + parts[9].off);
     *out = plan;
     return TA_OK;
 }
@@ -185,6 +188,15 @@ void tree_attn_plan_destroy(ta_plan *plan) {
 }
 
 size_t tree_attn_bwd_workspace_size(const ta_plan *plan) { return plan ? plan->ws_bytes : 0; }
+
+int tree_attn_set_trace_events(ta_plan *plan, void *const *events, int n_events) {
+    if (!plan || (events && n_events != 7)) {
+        set_error("tree_attn_set_trace_events: NULL plan or n_events != 7");
+        return TA_ERR_INVALID;
+    }
+    for (int i = 0; i < 7; ++i) plan->trace[i] = events ? events[i] : nullptr;
+    return TA_OK;
+}
 
 int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out) {
     if (!plan || !out) {
@@ -283,6 +295,7 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.entries = plan->d_entries;
     p.order = plan->d_fwd_order;
     p.page_table = plan->d_page_table;
+    p.tile_rows = plan->d_tile_rows;
     p.n_logical_pages = int32_t(h.n_logical_pages);
     p.num_pages = int32_t(h.cfg.num_pages);
     p.page_size = h.cfg.page_size;
@@ -296,7 +309,7 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.lse = lse;
     p.status = plan->d_status;
     cudaError_t e = launch_fwd(h.cfg.head_dim, tm_q, tm_k, tm_v, p, int(h.blocks.size() / 4),
-                               static_cast<cudaStream_t>(stream));
+                               static_cast<cudaStream_t>(stream), plan->trace);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
     return TA_OK;
 }
@@ -335,6 +348,8 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.reduce = plan->d_reduce;
     p.order = plan->d_fwd_order;
     p.page_table = plan->d_page_table;
+    p.tile_rows = plan->d_tile_rows;
+    p.t_info = plan->d_t_info;
     p.n_logical_pages = int32_t(h.n_logical_pages);
     p.num_pages = int32_t(c.num_pages);
     p.page_size = c.page_size;
@@ -355,7 +370,8 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.dv_pool = dv_pool;
     p.status = plan->d_status + 1;
     cudaError_t e = launch_bwd(c.head_dim, tm_q, tm_k, tm_v, tm_do, p, int(h.blocks.size() / 4),
-                               int(h.chunks.size() / 4), int(h.reduce.size() / 4), static_cast<cudaStream_t>(stream));
+                               int(h.chunks.size() / 4), int(h.reduce.size() / 4), static_cast<cudaStream_t>(stream),
+                               plan->trace);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attn_bwd launch");
     return TA_OK;
 }

@@ -44,18 +44,6 @@ __global__ void __launch_bounds__(256) delta_kernel(const BwdParams p) {
     if (lane == 0) p.delta[static_cast<size_t>(h) * p.N + r] = acc;
 }
 
-__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *tm, int tile, int g, int D,
-                                             const int32_t *page_table, int n_logical, int num_pages, int P,
-                                             uint32_t bar) {
-    const int pages = kTileRows / P;
-    for (int i = 0; i < pages; ++i) {
-        const int l = tile * pages + i;
-        const int y = l < n_logical ? __ldg(page_table + l) * P : num_pages * P;
-        for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(dst + c * (kTileRows * 128) + i * P * 128, tm, g * D + c * 64, y, bar);
-    }
-}
-
 // One 128-lane query tile t of a block: rows (head, row) flattened as m = hl * R + rl.
 __device__ __forceinline__ void load_q_tile(uint32_t dst, const CUtensorMap *tm, int t, int g, int G, int R,
                                             int D, int q_row0, uint32_t bar) {
@@ -77,34 +65,46 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t 
     }
 }
 
-template <int D>
-__device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc, bool acc) {
-    // D[128 x D] (+)= A[128 x 128] (bf16 in TMEM) * B[128 x D] (MN-major tile in smem)
+template <int D, int KROWS>
+__device__ __forceinline__ void issue_tn_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc, bool acc) {
+    // D[128 x D] (+)= A[128 x KROWS] (bf16 in TMEM) * B[KROWS x D] (rows of an MN-major tile)
 #pragma unroll
-    for (int kk = 0; kk < kTileRows / 16; ++kk)
+    for (int kk = 0; kk < KROWS / 16; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(sB + kk * 16 * 128, kTileRows * 128, 1024), idesc,
                (acc || kk > 0) ? 1u : 0u);
 }
 
-// ------------------------------------------------------------------------------ dQ
-constexpr int kDqThreads = 192;   // warps 0-3 elementwise, 4 TMA, 5 MMA
-constexpr int kStages = 2;
+// Both backward kernels split every 128-column S / dP tile into two 64-column halves,
+// double-buffered in TMEM, each half owned by one elementwise warpgroup: while one group
+// turns its half of S and dP into P / dS, the tensor core runs the other half's
+// accumulations and the next half's S and dP.
+constexpr int kBwdThreads = 320;   // warps 0-3 half a, 4-7 half b, 8 loads, 9 MMA
+constexpr int kStages = 2;         // dK/dV: Q/dO stages
+constexpr int kKStages = 3;        // dQ: K stages (K is held until the dQ MMAs)
+constexpr int kVStages = 2;        // dQ: V stages (V is released after the dP MMAs)
+// TMEM columns of the two half buffers: S_w [256+128w, 320+128w), dP_w [320+128w, 384+128w)
+__host__ __device__ constexpr uint32_t col_s(int w) { return 256u + 128u * w; }
+__host__ __device__ constexpr uint32_t col_dp(int w) { return 320u + 128u * w; }
 
+// ------------------------------------------------------------------------------ dQ
 template <int D>
 struct DqLayout {
     static constexpr int kTile = 128 * D * 2;
     static constexpr int q_off = 0;
     static constexpr int do_off = q_off + kTile;
     static constexpr int k_off = do_off + kTile;
-    static constexpr int v_off = k_off + kStages * kTile;
-    static constexpr int bar_off = v_off + kStages * kTile;
-    static constexpr int n_bars = 1 + 4 * kStages + 3;
+    static constexpr int v_off = k_off + kKStages * kTile;
+    static constexpr int bar_off = v_off + kVStages * kTile;
+    static constexpr int n_bars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;
 };
 
+// One CTA = one 128-lane query tile (t) of one query block x one KV head.  Per key-tile
+// entry: S_w = Q K_w^T, dP_w = dO V_w^T for the two 64-row halves w of the key tile, then
+// dS_w = P_w (dP_w - delta) back into TMEM as bf16 and dQ += dS_w K_w.
 template <int D>
-__global__ void __launch_bounds__(kDqThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
     using L = DqLayout<D>;
@@ -123,26 +123,25 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
     const uint32_t q_full = bar(0);
     auto k_full = [&](int s) { return bar(1 + s); };
-    auto k_empty = [&](int s) { return bar(1 + kStages + s); };
-    auto v_full = [&](int s) { return bar(1 + 2 * kStages + s); };
-    auto v_empty = [&](int s) { return bar(1 + 3 * kStages + s); };
-    const uint32_t s_full = bar(1 + 4 * kStages), p_full = bar(2 + 4 * kStages), o_full = bar(3 + 4 * kStages);
+    auto k_empty = [&](int s) { return bar(1 + kKStages + s); };
+    auto v_full = [&](int s) { return bar(1 + 2 * kKStages + s); };
+    auto v_empty = [&](int s) { return bar(1 + 2 * kKStages + kVStages + s); };
+    auto s_full = [&](int w) { return bar(1 + 2 * kKStages + 2 * kVStages + w); };
+    auto p_full = [&](int w) { return bar(3 + 2 * kKStages + 2 * kVStages + w); };
+    const uint32_t o_full = bar(5 + 2 * kKStages + 2 * kVStages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1);
-            mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1);
-        }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        for (int s = 0; s < kKStages; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
+        for (int s = 0; s < kVStages; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
+        for (int w = 0; w < 2; ++w) { mbar_init(s_full(w), 1); mbar_init(p_full(w), 128); }
         mbar_init(o_full, 1);
         *abort = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -150,61 +149,96 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns: S [0,128) | dP [128,256) (dS overwrites its first half) | dQ [256, 256+D)
-    constexpr uint32_t cS = 0, cDP = 128, cDQ = 256;
+    constexpr uint32_t cDQ = 0;      // dQ [0, D)
 
-    if (warp == 4) {
+    if (warp == 8) {
+        const int ppt = kTileRows / p.page_size;
         if (lane == 0) {
             tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
             tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
             mbar_arrive_expect_tx(q_full, 2 * L::kTile);
             load_q_tile(sQ, &tm_q, t, g, p.G, p.R, D, q_row0, q_full);
             load_q_tile(sDO, &tm_do, t, g, p.G, p.R, D, q_row0, q_full);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < E; ++j) {
-                const int tile = __ldg(&entries[j].x), s = j % kStages;
-                if (j >= kStages && !mbar_wait(k_empty(s), ((j / kStages) - 1) & 1, abort, p.status)) break;
-                mbar_arrive_expect_tx(k_full(s), L::kTile);
-                load_kv_tile(sK + s * L::kTile, &tm_k, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages,
-                             p.page_size, k_full(s));
-                k_issued = j + 1;
-                if (j >= kStages && !mbar_wait(v_empty(s), ((j / kStages) - 1) & 1, abort, p.status)) break;
-                mbar_arrive_expect_tx(v_full(s), L::kTile);
-                load_kv_tile(sV + s * L::kTile, &tm_v, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages,
-                             p.page_size, v_full(s));
-                v_issued = j + 1;
+        }
+        EntryFeed f;
+        int k_issued = 0, v_issued = 0;
+        for (int j = 0; j < E; ++j) {
+            if ((j & 31) == 0) feed_fill(f, j, E, entries, p.tile_rows, ppt, lane);
+            int y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, f.y[i], j & 31);
+            const int ks = j % kKStages, vs = j % kVStages;
+            bool ok = true;
+            if (lane == 0 && j >= kKStages) ok = mbar_wait(k_empty(ks), ((j / kKStages) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(k_full(ks), L::kTile);
+                tma_kv_tile(sK + ks * L::kTile, &tm_k, y, ppt, p.page_size, g, D, k_full(ks));
             }
-            for (int d = (k_issued > kStages ? k_issued - kStages : 0); d < k_issued; ++d)
-                mbar_wait(k_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
-            for (int d = (v_issued > kStages ? v_issued - kStages : 0); d < v_issued; ++d)
-                mbar_wait(v_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
+            k_issued = j + 1;
+            if (lane == 0 && j >= kVStages) ok = mbar_wait(v_empty(vs), ((j / kVStages) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(v_full(vs), L::kTile);
+                tma_kv_tile(sV + vs * L::kTile, &tm_v, y, ppt, p.page_size, g, D, v_full(vs));
+            }
+            v_issued = j + 1;
+        }
+        if (lane == 0) {
+            for (int d = (k_issued > kKStages ? k_issued - kKStages : 0); d < k_issued; ++d)
+                mbar_wait(k_full(d % kKStages), (d / kKStages) & 1, nullptr, p.status);
+            for (int d = (v_issued > kVStages ? v_issued - kVStages : 0); d < v_issued; ++d)
+                mbar_wait(v_full(d % kVStages), (d / kVStages) & 1, nullptr, p.status);
             mbar_wait(q_full, 0, nullptr, p.status);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16(128, kTileRows, 0, 0);
+            constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            bool ok = E > 0 && mbar_wait(q_full, 0, abort, p.status);
+            // S_w = Q K_w^T and dP_w = dO V_w^T for key rows [64w, 64w + 64) of stage s
+            auto issue_sdp = [&](int w, int ks, int vs) {
+                issue_qk<D>(tmem + col_s(w), sQ, sK + ks * L::kTile + w * 8192, idesc_s);
+                issue_qk<D>(tmem + col_dp(w), sDO, sV + vs * L::kTile + w * 8192, idesc_s);
+            };
+            bool ok = E > 0 && mbar_wait(q_full, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status) &&
+                      mbar_wait(v_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0, 0, 0);
+                mma_commit(s_full(0));
+                issue_sdp(1, 0, 0);
+                mma_commit(s_full(1));
+                mma_commit(v_empty(0));
+            }
             for (int j = 0; ok && j < E; ++j) {
-                const int s = j % kStages, ph = (j / kStages) & 1;
-                if (!(ok = mbar_wait(k_full(s), ph, abort, p.status))) break;
-                if (!(ok = mbar_wait(v_full(s), ph, abort, p.status))) break;
+                const int ks = j % kKStages, ks1 = (j + 1) % kKStages, vs1 = (j + 1) % kVStages;
+                if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_qk<D>(tmem + cS, sQ, sK + s * L::kTile, idesc_s);
-                issue_qk<D>(tmem + cDP, sDO, sV + s * L::kTile, idesc_s);
-                mma_commit(s_full);
-                mma_commit(v_empty(s));
-                if (!(ok = mbar_wait(p_full, j & 1, abort, p.status))) break;
+                issue_tn_k<D, 64>(tmem + cDQ, tmem + col_dp(0), sK + ks * L::kTile, idesc_o, j > 0);
+                if (j + 1 < E) {
+                    if (!(ok = mbar_wait(k_full(ks1), ((j + 1) / kKStages) & 1, abort, p.status) &&
+                               mbar_wait(v_full(vs1), ((j + 1) / kVStages) & 1, abort, p.status)))
+                        break;
+                    tc_fence_after();
+                    issue_sdp(0, ks1, vs1);
+                    mma_commit(s_full(0));
+                }
+                if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_tn<D>(tmem + cDQ, tmem + cDP, sK + s * L::kTile, idesc_o, j > 0);
-                mma_commit(k_empty(s));
+                issue_tn_k<D, 64>(tmem + cDQ, tmem + col_dp(1), sK + ks * L::kTile + 64 * 128, idesc_o, true);
+                mma_commit(k_empty(ks));
+                if (j + 1 < E) {
+                    issue_sdp(1, ks1, vs1);
+                    mma_commit(s_full(1));
+                    mma_commit(v_empty(vs1));
+                }
             }
             mma_commit(o_full);
             mbar_wait(o_full, 0, nullptr, p.status);
         }
     } else {
-        // ---------------------------------------------------------------- elementwise (warps 0-3)
-        const int q4 = warp;
+        // ---------------------------------------------------------------- elementwise (warps 0-7)
+        const int w = warp >> 2, q4 = warp & 3;
         const int m_flat = 128 * t + 32 * q4 + lane;
         const int hl = m_flat / p.R, rl = m_flat % p.R;
         const int r_abs = q_row0 + rl, h = g * p.G + hl;
@@ -216,43 +250,48 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         bool ok = true;
         for (int j = 0; j < E; ++j) {
             const int4 e = __ldg(&entries[j]);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort, p.status));
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
-            const int j0 = e.x * kTileRows;
+            const int j0 = e.x * kTileRows + 64 * w;
             const int hi = (e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z;
+            uint32_t sv[2][32], dpv[2][32];
 #pragma unroll
-            for (int c = 0; c < kTileRows / 32; ++c) {
-                uint32_t sv[32], dpv[32], ds[16];
-                tmem_ld32(tmem + lane_off + cS + 32 * c, sv);
-                tmem_ld32(tmem + lane_off + cDP + 32 * c, dpv);
-                tmem_wait_ld();
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld32(tmem + lane_off + col_s(w) + 32 * c, sv[c]);
+                tmem_ld32(tmem + lane_off + col_dp(w) + 32 * c, dpv[c]);
+            }
+            tmem_wait_ld();                          // one TMEM round trip per half
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t ds[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float pr[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int jj = j0 + 32 * c + 2 * i + u;
-                        const float pv = ex2(fmaf(__uint_as_float(sv[2 * i + u]), sl2, -lse2));
+                        const float pv = ex2(fmaf(__uint_as_float(sv[c][2 * i + u]), sl2, -lse2));
                         const bool vis = e.w == 0 || (jj >= e.y && jj < hi);
-                        pr[u] = vis ? pv * (__uint_as_float(dpv[2 * i + u]) - delta) : 0.f;
+                        pr[u] = vis ? pv * (__uint_as_float(dpv[c][2 * i + u]) - delta) : 0.f;
                     }
                     ds[i] = pack_bf16(pr[0], pr[1]);
                 }
-                tmem_st16(tmem + lane_off + cDP + 16 * c, ds);
+                tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, ds);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full(w));
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
             tc_fence_after();
-            float *dst = p.dq + (static_cast<size_t>(r_abs) * p.Hq + h) * D;
+            // each group writes half of the row's columns
+            float *dst = p.dq + (static_cast<size_t>(r_abs) * p.Hq + h) * D + w * (D / 2);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_off + cDQ + 32 * c, v);
+                tmem_ld32(tmem + lane_off + cDQ + w * (D / 2) + 32 * c, v);
                 tmem_wait_ld();
                 if (valid) {
                     float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * c);
@@ -266,15 +305,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
 
 // ------------------------------------------------------------------------------ dK, dV
-constexpr int kKvThreads = 192;   // warps 0-3 elementwise, 4 loads, 5 MMA
-
 template <int D>
 struct DkvLayout {
     static constexpr int kTile = 128 * D * 2;
@@ -283,13 +320,17 @@ struct DkvLayout {
     static constexpr int q_off = v_off + kTile;                 // stage s: Q at q_off + s*2*kTile, dO after it
     static constexpr int lse_off = q_off + kStages * 2 * kTile; // stage s: 128 lse2 + 128 delta + 128 rows
     static constexpr int bar_off = lse_off + kStages * 3 * 128 * 4;
-    static constexpr int n_bars = 1 + 2 * kStages + 3;
+    static constexpr int n_bars = 1 + 2 * kStages + 2 + 2 + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;
 };
 
+// One CTA = one key tile x one KV head x one chunk of the tile's readers.  K and V stay in
+// shared memory; for every (reader block, 128-lane query tile): S^T_w = K Q_w^T and
+// dP^T_w = V dO_w^T for the two 64-lane halves w of the query tile, P^T_w and dS^T_w back
+// into TMEM as bf16, then dV += P^T_w dO_w and dK += dS^T_w Q_w, accumulated in TMEM.
 template <int D>
-__global__ void __launch_bounds__(kKvThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
     using L = DkvLayout<D>;
@@ -301,7 +342,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int ci = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
     const int tile = __ldg(p.chunks + 4 * ci), a0 = __ldg(p.chunks + 4 * ci + 1);
     const int n_ent = __ldg(p.chunks + 4 * ci + 2) - a0, slot = __ldg(p.chunks + 4 * ci + 3);
-    const int4 *tents = reinterpret_cast<const int4 *>(p.t_entries) + a0;
+    const int4 *tinfo = reinterpret_cast<const int4 *>(p.t_info) + a0;   // first row, rows<<8|flags, lo, hi
     const int U = 2 * n_ent;   // (entry, query tile) units
 
     const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off;
@@ -312,20 +353,21 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t kv_full = bar(0);
     auto qd_full = [&](int s) { return bar(1 + s); };
     auto qd_empty = [&](int s) { return bar(1 + kStages + s); };
-    const uint32_t s_full = bar(1 + 2 * kStages), p_full = bar(2 + 2 * kStages), o_full = bar(3 + 2 * kStages);
+    auto s_full = [&](int w) { return bar(1 + 2 * kStages + w); };
+    auto p_full = [&](int w) { return bar(3 + 2 * kStages + w); };
+    const uint32_t o_full = bar(5 + 2 * kStages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < kStages; ++s) { mbar_init(qd_full(s), 1); mbar_init(qd_empty(s), 1); }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        for (int w = 0; w < 2; ++w) { mbar_init(s_full(w), 1); mbar_init(p_full(w), 128); }
         mbar_init(o_full, 1);
         *abort = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -333,38 +375,51 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns: S^T [0,128) (P^T overwrites its first half) | dP^T [128,256) (dS^T likewise)
-    //               | dV [256, 256+D) | dK [256+D, 256+2D)
-    constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
+    constexpr uint32_t cDV = 0, cDK = D;   // dV [0, D), dK [D, 2D)
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ---------------------------------------------------------------- loads (whole warp)
+        const int ppt = kTileRows / p.page_size;
+        int ky[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ky[i] = i < ppt ? __ldg(p.tile_rows + tile * ppt + i) : 0;
         if (lane == 0) {
             tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
             tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
             mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
-            load_kv_tile(sK, &tm_k, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages, p.page_size, kv_full);
-            load_kv_tile(sV, &tm_v, tile, g, D, p.page_table, p.n_logical_pages, p.num_pages, p.page_size, kv_full);
+            tma_kv_tile(sK, &tm_k, ky, ppt, p.page_size, g, D, kv_full);
+            tma_kv_tile(sV, &tm_v, ky, ppt, p.page_size, g, D, kv_full);
         }
+        const int log2R = 31 - __clz(p.R);
+        int4 mine = make_int4(0, 0, 0, 0);   // lane i holds the reader info of entry (base + i)
         int issued = 0;
         for (int u = 0; u < U; ++u) {
-            const int s = u % kStages, t = u & 1;
+            const int s = u % kStages, t = u & 1, e = u >> 1;
+            if ((u & 63) == 0 && e + lane < n_ent) mine = __ldg(tinfo + e + lane);
+            const int q_row0 = __shfl_sync(0xffffffffu, mine.x, e & 31);
+            const int n_rows = __shfl_sync(0xffffffffu, mine.y, e & 31) >> 8;
+            // issue every lse / delta load before the first shared-memory store
+            float lv[4], dl[4];
+            int rr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m_flat = 128 * t + lane + 32 * i;
+                const int hl = m_flat >> log2R, rl = m_flat & (p.R - 1);
+                const size_t idx = static_cast<size_t>(g * p.G + hl) * p.N + q_row0 + rl;
+                const bool valid = rl < n_rows;
+                lv[i] = valid ? __ldg(p.lse + idx) * kLog2e : INFINITY;      // +inf: P = 0 for padding rows
+                dl[i] = valid ? __ldg(p.delta + idx) : 0.f;
+                rr[i] = q_row0 + rl;
+            }
             bool ok = true;
             if (lane == 0 && u >= kStages) ok = mbar_wait(qd_empty(s), ((u / kStages) - 1) & 1, abort, p.status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-            const int4 te = __ldg(&tents[u >> 1]);
-            const int qb = te.x;
-            const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
             float *ls = lse_s + s * 3 * 128;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int m = lane + 32 * i, m_flat = 128 * t + m;
-                const int hl = m_flat / p.R, rl = m_flat % p.R, h = g * p.G + hl;
-                const bool valid = rl < n_rows;
-                const size_t idx = static_cast<size_t>(h) * p.N + q_row0 + rl;
-                ls[m] = valid ? __ldg(p.lse + idx) * kLog2e : INFINITY;      // +inf: P = 0 for padding rows
-                ls[128 + m] = valid ? p.delta[idx] : 0.f;
-                reinterpret_cast<int *>(ls)[256 + m] = q_row0 + rl;
+                ls[lane + 32 * i] = lv[i];
+                ls[128 + lane + 32 * i] = dl[i];
+                reinterpret_cast<int *>(ls)[256 + lane + 32 * i] = rr[i];
             }
             __syncwarp();
             if (lane == 0) {
@@ -379,30 +434,54 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mbar_wait(qd_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
             mbar_wait(kv_full, 0, nullptr, p.status);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status);
+            // S^T_w = K Q_w^T, dP^T_w = V dO_w^T for query lanes [64w, 64w + 64) of stage s
+            auto issue_sdp = [&](int w, int s) {
+                issue_qk<D>(tmem + col_s(w), sK, sQ(s) + w * 8192, idesc_s);
+                issue_qk<D>(tmem + col_dp(w), sV, sDO(s) + w * 8192, idesc_s);
+            };
+            // dV += P^T_w dO_w, dK += dS^T_w Q_w (64 query lanes of stage s)
+            auto issue_acc = [&](int w, int s, bool acc) {
+                issue_tn_k<D, 64>(tmem + cDV, tmem + col_s(w), sDO(s) + w * 8192, idesc_o, acc);
+                issue_tn_k<D, 64>(tmem + cDK, tmem + col_dp(w), sQ(s) + w * 8192, idesc_o, acc);
+            };
+            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(qd_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0, 0);
+                mma_commit(s_full(0));
+                issue_sdp(1, 0);
+                mma_commit(s_full(1));
+            }
             for (int u = 0; ok && u < U; ++u) {
-                const int s = u % kStages;
-                if (!(ok = mbar_wait(qd_full(s), (u / kStages) & 1, abort, p.status))) break;
+                const int s = u % kStages, s1 = (u + 1) % kStages;
+                if (!(ok = mbar_wait(p_full(0), u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_qk<D>(tmem + cS, sK, sQ(s), idesc_s);       // S^T = K Q^T
-                issue_qk<D>(tmem + cDP, sV, sDO(s), idesc_s);     // dP^T = V dO^T
-                mma_commit(s_full);
-                if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
+                issue_acc(0, s, u > 0);
+                if (u + 1 < U) {
+                    if (!(ok = mbar_wait(qd_full(s1), ((u + 1) / kStages) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    issue_sdp(0, s1);
+                    mma_commit(s_full(0));
+                }
+                if (!(ok = mbar_wait(p_full(1), u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_tn<D>(tmem + cDV, tmem + cS, sDO(s), idesc_o, u > 0);    // dV += P^T dO
-                issue_tn<D>(tmem + cDK, tmem + cDP, sQ(s), idesc_o, u > 0);    // dK += dS^T Q
+                issue_acc(1, s, true);
                 mma_commit(qd_empty(s));
+                if (u + 1 < U) {
+                    issue_sdp(1, s1);
+                    mma_commit(s_full(1));
+                }
             }
             mma_commit(o_full);
             mbar_wait(o_full, 0, nullptr, p.status);
         }
     } else {
-        // ---------------------------------------------------------------- elementwise (warps 0-3)
-        const int q4 = warp;
+        // ---------------------------------------------------------------- elementwise (warps 0-7)
+        const int w = warp >> 2, q4 = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const int row = 32 * q4 + lane;                 // key row within the tile
         const int jj = tile * kTileRows + row;          // its compact row
@@ -410,80 +489,80 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         bool ok = true;
         for (int u = 0; u < U; ++u) {
             const int s = u % kStages;
-            const int4 te = __ldg(&tents[u >> 1]);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, abort, p.status));
+            const int4 te = __ldg(&tinfo[u >> 1]);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), u & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
-            const float *ls = lse_s + s * 3 * 128;
-            const int *rs = reinterpret_cast<const int *>(ls) + 256;
-            const bool row_in = jj >= te.y && jj < te.z;
-            const bool causal = (te.w & kEntryCausal) != 0;
+            const float *ls = lse_s + s * 3 * 128 + 64 * w;
+            const int *rs = reinterpret_cast<const int *>(lse_s + s * 3 * 128) + 256 + 64 * w;
+            const bool row_in = jj >= te.z && jj < te.w;
+            const bool causal = (te.y & kEntryCausal) != 0;
+            uint32_t sv[2][32], dpv[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sv[32], dpv[32], pk[16], dk[16];
-                tmem_ld32(tmem + lane_off + cS + 32 * c, sv);
-                tmem_ld32(tmem + lane_off + cDP + 32 * c, dpv);
-                tmem_wait_ld();
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld32(tmem + lane_off + col_s(w) + 32 * c, sv[c]);
+                tmem_ld32(tmem + lane_off + col_dp(w) + 32 * c, dpv[c]);
+            }
+            tmem_wait_ld();                          // one TMEM round trip per half
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float pr[2], dr[2];
 #pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int m = 32 * c + 2 * i + w;
-                        float pv = ex2(fmaf(__uint_as_float(sv[2 * i + w]), sl2, -ls[m]));
+                    for (int v = 0; v < 2; ++v) {
+                        const int m = 32 * c + 2 * i + v;
+                        float pv = ex2(fmaf(__uint_as_float(sv[c][2 * i + v]), sl2, -ls[m]));
                         if (!row_in || (causal && jj > rs[m])) pv = 0.f;
-                        pr[w] = pv;
-                        dr[w] = pv * (__uint_as_float(dpv[2 * i + w]) - ls[128 + m]);
+                        pr[v] = pv;
+                        dr[v] = pv * (__uint_as_float(dpv[c][2 * i + v]) - ls[128 + m]);
                     }
                     pk[i] = pack_bf16(pr[0], pr[1]);
                     dk[i] = pack_bf16(dr[0], dr[1]);
                 }
-                tmem_st16(tmem + lane_off + cS + 16 * c, pk);
-                tmem_st16(tmem + lane_off + cDP + 16 * c, dk);
+                tmem_st16(tmem + lane_off + col_s(w) + 16 * c, pk);
+                tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, dk);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full(w));
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
             tc_fence_after();
-            float *dk_dst, *dv_dst;
+            // group 0 writes dK (scaled), group 1 writes dV
+            float *dst;
             bool write = true;
             if (slot >= 0) {
-                float *base = p.partials + (static_cast<size_t>(slot) * p.Hkv + g) * 2 * kTileRows * D;
-                dk_dst = base + static_cast<size_t>(row) * D;
-                dv_dst = base + static_cast<size_t>(kTileRows + row) * D;
+                dst = p.partials + (static_cast<size_t>(slot) * p.Hkv + g) * 2 * kTileRows * D +
+                      static_cast<size_t>(w * kTileRows + row) * D;
             } else {
                 write = jj < p.N;
                 const int l = jj / p.page_size;
                 const size_t prow = write ? static_cast<size_t>(__ldg(p.page_table + l)) * p.page_size + jj % p.page_size : 0;
-                dk_dst = p.dk_pool + (prow * p.Hkv + g) * D;
-                dv_dst = p.dv_pool + (prow * p.Hkv + g) * D;
+                dst = (w == 0 ? p.dk_pool : p.dv_pool) + (prow * p.Hkv + g) * D;
             }
+            const float mul = w == 0 ? p.scale : 1.f;
+            const uint32_t src = tmem + lane_off + (w == 0 ? cDK : cDV);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t kv[32], vv[32];
-                tmem_ld32(tmem + lane_off + cDK + 32 * c, kv);
-                tmem_ld32(tmem + lane_off + cDV + 32 * c, vv);
+                uint32_t v[32];
+                tmem_ld32(src + 32 * c, v);
                 tmem_wait_ld();
                 if (write) {
-                    float4 *k4 = reinterpret_cast<float4 *>(dk_dst + 32 * c);
-                    float4 *v4 = reinterpret_cast<float4 *>(dv_dst + 32 * c);
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * c);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        k4[i] = make_float4(__uint_as_float(kv[4 * i]) * p.scale, __uint_as_float(kv[4 * i + 1]) * p.scale,
-                                            __uint_as_float(kv[4 * i + 2]) * p.scale, __uint_as_float(kv[4 * i + 3]) * p.scale);
-                        v4[i] = make_float4(__uint_as_float(vv[4 * i]), __uint_as_float(vv[4 * i + 1]),
-                                            __uint_as_float(vv[4 * i + 2]), __uint_as_float(vv[4 * i + 3]));
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
+                                            __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -517,23 +596,28 @@ __global__ void __launch_bounds__(256) reduce_kernel(const BwdParams p) {
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                          const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, void *const *trace) {
     const long long rows = static_cast<long long>(p.N) * p.Hq;
+    trace_record(trace, 2, stream);
     delta_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::bytes);
     if (e != cudaSuccess) return e;
-    dq_kernel<D><<<n_blocks * p.Hkv * 2, kDqThreads, DqLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    trace_record(trace, 3, stream);
+    dq_kernel<D><<<n_blocks * p.Hkv * 2, kBwdThreads, DqLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::bytes);
     if (e != cudaSuccess) return e;
-    dkdv_kernel<D><<<n_chunks * p.Hkv, kKvThreads, DkvLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    trace_record(trace, 4, stream);
+    dkdv_kernel<D><<<n_chunks * p.Hkv, kBwdThreads, DkvLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    trace_record(trace, 5, stream);
     if (n_reduce > 0) {
         reduce_kernel<D><<<n_reduce * p.Hkv, 256, 0, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    trace_record(trace, 6, stream);
     return cudaSuccess;
 }
 
@@ -541,9 +625,9 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
 
 cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
-                       cudaStream_t stream) {
-    if (D == 64) return launch_bwd_d<64>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream);
-    return launch_bwd_d<128>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream);
+                       cudaStream_t stream, void *const *trace) {
+    if (D == 64) return launch_bwd_d<64>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream, trace);
+    return launch_bwd_d<128>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream, trace);
 }
 
 }  // namespace treeattn

@@ -307,20 +307,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 template <int D>
 cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                         const FwdParams &p, int n_blocks, cudaStream_t stream) {
+                         const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace) {
     const int smem = FwdLayout<D>::bytes;
     cudaError_t err = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
+    trace_record(trace, 0, stream);
     fwd_kernel<D><<<n_blocks * p.Hkv, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
-    return cudaGetLastError();
+    err = cudaGetLastError();
+    trace_record(trace, 1, stream);
+    return err;
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const FwdParams &p, int n_blocks, cudaStream_t stream) {
-    if (D == 64) return launch_fwd_d<64>(tm_q, tm_k, tm_v, p, n_blocks, stream);
-    return launch_fwd_d<128>(tm_q, tm_k, tm_v, p, n_blocks, stream);
+                       const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace) {
+    if (D == 64) return launch_fwd_d<64>(tm_q, tm_k, tm_v, p, n_blocks, stream, trace);
+    return launch_fwd_d<128>(tm_q, tm_k, tm_v, p, n_blocks, stream, trace);
 }
 
 }  // namespace treeattn

@@ -13,6 +13,7 @@ struct FwdParams {
     const int32_t *entries;     // 4 per entry: key tile, lo, hi, flags
     const int32_t *order;       // query blocks, longest first
     const int32_t *page_table;  // logical page -> pool page
+    const int32_t *tile_rows;   // per key tile, per page: pool row of the page (TMA y)
     int32_t n_logical_pages;
     int32_t num_pages;
     int32_t page_size;
@@ -32,6 +33,8 @@ struct BwdParams {
     const int32_t *reduce;      // 4 per split tile: tile, first slot, slots, 0
     const int32_t *order;
     const int32_t *page_table;
+    const int32_t *tile_rows;
+    const int32_t *t_info;      // per tile-major entry: first row, rows << 8 | flags, lo, hi
     int32_t n_logical_pages;
     int32_t num_pages;
     int32_t page_size;
@@ -50,11 +53,16 @@ struct BwdParams {
     int *status;
 };
 
+// `trace`: NULL, or cudaEvent_t handles (entries may be NULL) recorded around the launches.
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const FwdParams &p, int n_blocks, cudaStream_t stream);
+                       const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace);
 
 cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks,
-                       int n_reduce, cudaStream_t stream);
+                       int n_reduce, cudaStream_t stream, void *const *trace);
+
+inline void trace_record(void *const *trace, int i, cudaStream_t s) {
+    if (trace && trace[i]) cudaEventRecord(static_cast<cudaEvent_t>(trace[i]), s);
+}
 
 }  // namespace treeattn

@@ -388,6 +388,25 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
     });
     for (auto &x : ch) P.chunks.insert(P.chunks.end(), {(int32_t)x[0], (int32_t)x[1], (int32_t)x[2], (int32_t)x[3]});
 
+    // device-side helpers: TMA rows of every tile's pages; reader info per tile-major entry
+    {
+        const int ppt = T / Pg;
+        P.tile_rows.assign(n_tiles * ppt, 0);
+        for (int64_t k = 0; k < n_tiles; ++k)
+            for (int i = 0; i < ppt; ++i) {
+                const int64_t l = k * ppt + i;
+                P.tile_rows[k * ppt + i] = l < need_pages ? P.page_table[l] * Pg : int32_t(c.num_pages * Pg);
+            }
+        P.t_info.assign(4 * n_entries, 0);
+        for (int64_t e = 0; e < n_entries; ++e) {
+            const int32_t b = P.t_entries[4 * e];
+            P.t_info[4 * e] = blocks[4 * b];
+            P.t_info[4 * e + 1] = (blocks[4 * b + 1] << 8) | P.t_entries[4 * e + 3];
+            P.t_info[4 * e + 2] = P.t_entries[4 * e + 1];
+            P.t_info[4 * e + 3] = P.t_entries[4 * e + 2];
+        }
+    }
+
     P.plan_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
     return TA_OK;
 }

@@ -36,6 +36,9 @@ struct HostPlan {
     std::vector<int32_t> fwd_order;   // block ids, longest first
     std::vector<int32_t> reduce;      // 4 per split tile: tile, first slot, slots, 0
     std::vector<int32_t> page_table;
+    std::vector<int32_t> tile_rows;   // per key tile, per page: TMA row of the page in the pool
+                                      // (pool rows; num_pages * P past the strip: zero fill)
+    std::vector<int32_t> t_info;      // per tile-major entry: first row, rows << 8 | flags, lo, hi
     int64_t n_segments = 0;
     int64_t n_partial_slots = 0;
     int64_t pairs = 0;
@@ -61,9 +64,12 @@ struct ta_plan {
     const int32_t *d_fwd_order = nullptr;
     const int32_t *d_reduce = nullptr;
     const int32_t *d_page_table = nullptr;
+    const int32_t *d_tile_rows = nullptr;
+    const int32_t *d_t_info = nullptr;
     int32_t *d_status = nullptr;      // bounded-wait status words (zeroed at plan time)
     size_t ws_delta_bytes = 0;        // workspace: delta [Hq, N] fp32, 256-aligned
     size_t ws_bytes = 0;              // total bwd workspace
     int device = 0;
     int num_sms = 0;
+    void *trace[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};  // cudaEvent_t
 };

@@ -202,6 +202,36 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Warp-cooperative prefetch of key-tile entries: lane i holds entry (base + i) of the list and
+// the pool rows of its tile's pages, so one round trip serves 32 entries; the producer loop
+// reads them with shuffles.  pages_per_tile <= 8.
+struct EntryFeed {
+    int4 e;
+    int y[8];
+};
+
+__device__ __forceinline__ void feed_fill(EntryFeed &f, int base, int n, const int4 *entries,
+                                          const int32_t *tile_rows, int ppt, int lane) {
+    const int j = base + lane;
+    if (j < n) {
+        f.e = __ldg(entries + j);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < ppt) f.y[i] = __ldg(tile_rows + f.e.x * ppt + i);
+    }
+}
+
+// TMA loads of one key tile (128 rows, `ppt` pages) of KV head g into a 128-row smem tile:
+// page i goes to rows [i*P, (i+1)*P), each 64-column chunk c to its own 16 KB half.
+__device__ __forceinline__ void tma_kv_tile(uint32_t dst, const void *tm, const int (&y)[8], int ppt, int P, int g,
+                                            int D, uint32_t bar) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < ppt)
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_2d(dst + c * (128 * 128) + i * P * 128, tm, g * D + c * 64, y[i], bar);
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -221,6 +221,13 @@ size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
  * (TA_ERR_CUDA); clears the status. */
 int tree_attn_check(const ta_plan *plan, void *stream);
 
+/* Optional per-kernel tracing.  With events set, tree_attn_fwd records events[0] before and
+ * events[1] after its kernel; tree_attn_bwd records events[2], [3], [4], [5] before its
+ * delta, dQ, dK/dV and reduce kernels and events[6] after the last one -- all on the call's
+ * stream (cudaEvent_t handles created and owned by the caller; entries may be NULL).  Pass
+ * events = NULL to stop.  n_events must be 7 unless events is NULL. */
+int tree_attn_set_trace_events(ta_plan *plan, void *const *events, int n_events);
+
 int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out);
 int tree_attn_plan_export(const ta_plan *plan, ta_plan_arrays *out);
 void tree_attn_plan_destroy(ta_plan *plan);
