@@ -98,6 +98,8 @@ def lib():
     L.tree_attn_fwd.restype = ctypes.c_int
     L.tree_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.tree_attn_bwd.restype = ctypes.c_int
+    L.tree_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.tree_attn_bwd_noalloc.restype = ctypes.c_int
     L.tree_attn_bwd_workspace_size.argtypes = [vp]
     L.tree_attn_bwd_workspace_size.restype = sz
     L.tree_attn_check.argtypes = [vp, vp]
@@ -197,6 +199,14 @@ def tree_attn_bwd(plan: Plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_po
     _check(lib().tree_attn_bwd(plan.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(o), _ptr(lse),
                                _ptr(d_o), _ptr(dq), _ptr(dk_pool), _ptr(dv_pool), _ptr(workspace),
                                int(ws_bytes), _stream(stream)))
+
+
+def tree_attn_bwd_noalloc(plan: Plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool,
+                          stream=None) -> None:
+    """tree_attn_bwd using the library's fixed scratch array instead of a workspace (for
+    callers that cannot allocate device memory; see include/treeattn.h)."""
+    _check(lib().tree_attn_bwd_noalloc(plan.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(o), _ptr(lse),
+                                       _ptr(d_o), _ptr(dq), _ptr(dk_pool), _ptr(dv_pool), _stream(stream)))
 
 
 def tree_attn_bwd_workspace_size(plan: Plan) -> int:

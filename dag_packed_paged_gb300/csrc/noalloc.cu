@@ -1,0 +1,87 @@
+// tree_attn_bwd_noalloc: the backward without a caller-provided workspace.
+//
+// Some callers cannot hand the library any device memory beyond the tensors of the call:
+// plugin-style hosts whose interface passes a kernel only its input and output buffers
+// (there is no hook to request scratch), and latency-critical loops that forbid device
+// allocation once they are running, because cudaMalloc can synchronise the device and a
+// fresh allocation may fail or fragment a carefully sized pool.  For them the backward's
+// scratch -- delta [Hq, N] fp32 and the dK/dV partial slots of key tiles whose readers
+// were split -- lives in one fixed array inside this library instead.
+//
+// The array below is a file-scope __device__ variable: every GPU that loads the library
+// holds all of it until the process exits.  In host code its name is only a host-side
+// stand-in, not a device address, so the entry point looks the address up with
+// cudaGetSymbolAddress (once per device, with that device current) and passes that pointer
+// on.  Nothing in it needs clearing: every byte the backward reads from the scratch is
+// written earlier in the same call.  All calls share the array, so calls whose kernels
+// overlap on the GPU (different streams, or different host threads) race on it.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "../../include/treeattn.h"
+#include "plan.h"
+
+namespace treeattn {
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB
+
+static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device (looked up on first use).
+int scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error(std::string("tree_attn_bwd_noalloc: cudaGetDevice: ") + cudaGetErrorString(e));
+        return TA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("tree_attn_bwd_noalloc: device index beyond the supported range");
+        return TA_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+        if (e != cudaSuccess || !ptr) {
+            set_error(std::string("tree_attn_bwd_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+            return TA_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return TA_OK;
+}
+
+}  // namespace
+}  // namespace treeattn
+
+extern "C" int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
+                                     const void *o, const float *lse, const void *d_o, float *dq, float *dk_pool,
+                                     float *dv_pool, void *stream) {
+    using namespace treeattn;
+    if (!plan) {
+        set_error("tree_attn_bwd_noalloc: plan is NULL");
+        return TA_ERR_INVALID;
+    }
+    const size_t need = tree_attn_bwd_workspace_size(plan);
+    if (need > kNoAllocScratchBytes) {
+        set_error("tree_attn_bwd_noalloc: this plan needs " + std::to_string(need) +
+                  " bytes of backward scratch, more than the " + std::to_string(kNoAllocScratchBytes) +
+                  " bytes the library holds for this entry point; call tree_attn_bwd with a workspace instead");
+        return TA_ERR_UNSUPPORTED;
+    }
+    void *scratch = nullptr;
+    const int rc = scratch_address(&scratch);
+    if (rc != TA_OK) return rc;
+    return tree_attn_bwd(plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, scratch, kNoAllocScratchBytes,
+                         stream);
+}

@@ -213,6 +213,25 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
                   const void *o, const float *lse, const void *d_o, float *dq, float *dk_pool,
                   float *dv_pool, void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * tree_attn_bwd_noalloc -- tree_attn_bwd without a caller-provided workspace.  The pages have
+ * no counterpart to this; it exists for callers that cannot give the library device scratch:
+ * plugin-style hosts that pass a kernel only its input and output buffers, and loops that
+ * forbid device allocation while running (cudaMalloc can synchronise the device and may fail
+ * or fragment a sized pool).  It allocates nothing.  The scratch (delta and dK/dV partials)
+ * is a fixed 64 MiB array inside the library that every GPU loading the library holds until
+ * the process exits; plans needing more (tree_attn_bwd_workspace_size(plan) > 64 MiB) are
+ * rejected with TA_ERR_UNSUPPORTED and a message naming the size.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  All calls share the array and nothing in it
+ * needs clearing between calls, so calls whose kernels overlap on the GPU (other streams or
+ * host threads) race on it: serialise them.  Arguments, outputs and other errors are those of
+ * tree_attn_bwd.
+ */
+int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
+                          const void *o, const float *lse, const void *d_o, float *dq, float *dk_pool,
+                          float *dv_pool, void *stream);
+
 /* Bytes of device scratch tree_attn_bwd needs for this plan (delta and dK/dV partials). */
 size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
 
