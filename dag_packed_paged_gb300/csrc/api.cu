@@ -360,6 +360,7 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.R = h.block_rows;
     p.scale = h.scale;
     p.scale_log2 = h.scale * 1.4426950408889634f;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
     p.o = static_cast<const __nv_bfloat16 *>(o);
     p.d_o = static_cast<const __nv_bfloat16 *>(d_o);
     p.lse = lse;

@@ -58,19 +58,22 @@ __device__ __forceinline__ void load_q_tile(uint32_t dst, const CUtensorMap *tm,
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t sB, uint32_t idesc) {
     // D[128 x 128] = A[128 x D] * B[128 x D]^T, both K-major 128-byte-swizzled tiles
+    // descriptors are built once; advancing along K only moves the 14-bit start-address field
+    const uint64_t a0 = sdesc_sw128(sA, 16, 1024), b0 = sdesc_sw128(sB, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
-        mma_ss(d_tmem, sdesc_sw128(sA + koff, 16, 1024), sdesc_sw128(sB + koff, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        const uint64_t koff = static_cast<uint64_t>(((kk >> 2) * (kTileRows * 128) + (kk & 3) * 32) >> 4);
+        mma_ss(d_tmem, a0 + koff, b0 + koff, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 template <int D, int KROWS>
 __device__ __forceinline__ void issue_tn_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc, bool acc) {
     // D[128 x D] (+)= A[128 x KROWS] (bf16 in TMEM) * B[KROWS x D] (rows of an MN-major tile)
+    const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
 #pragma unroll
     for (int kk = 0; kk < KROWS / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(sB + kk * 16 * 128, kTileRows * 128, 1024), idesc,
+        mma_ts(d_tmem, a_tmem + kk * 8, b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
                (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -81,18 +84,50 @@ __device__ __forceinline__ void issue_tn_k(uint32_t d_tmem, uint32_t a_tmem, uin
 constexpr int kBwdThreads = 320;   // warps 0-3 half a, 4-7 half b, 8 loads, 9 MMA
 constexpr int kStages = 2;         // dK/dV: Q/dO stages
 constexpr int kKStages = 3;        // dQ: K stages (K is held until the dQ MMAs)
-constexpr int kVStages = 2;        // dQ: V stages (V is released after the dP MMAs)
+constexpr int kVStages = 3;        // dQ: V stages (V is released after the dP MMAs)
 // TMEM columns of the two half buffers: S_w [256+128w, 320+128w), dP_w [320+128w, 384+128w)
 __host__ __device__ constexpr uint32_t col_s(int w) { return 256u + 128u * w; }
 __host__ __device__ constexpr uint32_t col_dp(int w) { return 320u + 128u * w; }
+
+template <int D>
+__device__ __forceinline__ void issue_tk(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc) {
+    // D[128 x N] = A[128 x D] (bf16 rows resident in TMEM) * B[N x D]^T (K-major smem tile):
+    // only B is read from shared memory
+    const uint64_t b0 = sdesc_sw128(sB, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8,
+               b0 + static_cast<uint64_t>(((kk >> 2) * (kTileRows * 128) + (kk & 3) * 32) >> 4), idesc,
+               kk > 0 ? 1u : 0u);
+}
+
+// Copy one bf16 row of D elements from global memory into this thread's TMEM lane at
+// column `col` (two elements per 32-bit column, the layout tcgen05.mma reads A from).
+template <int D>
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16 *row, bool valid) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        if (valid) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(row + 64 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 x = __ldg(src + i);
+                v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        tmem_st32(taddr + 32 * c, v);
+    }
+}
 
 // ------------------------------------------------------------------------------ dQ
 template <int D>
 struct DqLayout {
     static constexpr int kTile = 128 * D * 2;
-    static constexpr int q_off = 0;
-    static constexpr int do_off = q_off + kTile;
-    static constexpr int k_off = do_off + kTile;
+    static constexpr int k_off = 0;
     static constexpr int v_off = k_off + kKStages * kTile;
     static constexpr int bar_off = v_off + kVStages * kTile;
     static constexpr int n_bars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1;
@@ -100,9 +135,10 @@ struct DqLayout {
     static constexpr int bytes = misc_off + 16 + 1024;
 };
 
-// One CTA = one 128-lane query tile (t) of one query block x one KV head.  Per key-tile
-// entry: S_w = Q K_w^T, dP_w = dO V_w^T for the two 64-row halves w of the key tile, then
-// dS_w = P_w (dP_w - delta) back into TMEM as bf16 and dQ += dS_w K_w.
+// One CTA = one 128-lane query tile (t) of one query block x one KV head.  The tile's Q and
+// dO rows stay in TMEM for the CTA's lifetime, so S = Q K^T and dP = dO V^T read only the
+// key tile from shared memory.  Per key-tile entry: S_w, dP_w for the two 64-row halves w of
+// the key tile, dS_w = P_w (dP_w - delta) back into TMEM as bf16, then dQ += dS_w K_w.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -119,9 +155,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const int e0 = __ldg(p.blocks + 4 * qb + 2), E = __ldg(p.blocks + 4 * qb + 3) - e0;
     const int4 *entries = reinterpret_cast<const int4 *>(p.entries) + e0;
 
-    const uint32_t sQ = sbase + L::q_off, sDO = sbase + L::do_off, sK = sbase + L::k_off, sV = sbase + L::v_off;
+    const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off;
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
-    const uint32_t q_full = bar(0);
+    const uint32_t qd_ready = bar(0);
     auto k_full = [&](int s) { return bar(1 + s); };
     auto k_empty = [&](int s) { return bar(1 + kKStages + s); };
     auto v_full = [&](int s) { return bar(1 + 2 * kKStages + s); };
@@ -133,7 +169,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        mbar_init(qd_ready, 256);
         for (int s = 0; s < kKStages; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
         for (int w = 0; w < 2; ++w) { mbar_init(s_full(w), 1); mbar_init(p_full(w), 128); }
@@ -149,17 +185,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t cDQ = 0;      // dQ [0, D)
+    // TMEM columns: Q [0, D/2) and dO [64, 64 + D/2) as bf16 pairs, dQ [128, 128 + D),
+    // then the two S / dP half buffers
+    constexpr uint32_t cQ = 0, cDO = 64, cDQ = 128;
 
     if (warp == 8) {
         const int ppt = kTileRows / p.page_size;
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
-            tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(q_full, 2 * L::kTile);
-            load_q_tile(sQ, &tm_q, t, g, p.G, p.R, D, q_row0, q_full);
-            load_q_tile(sDO, &tm_do, t, g, p.G, p.R, D, q_row0, q_full);
-        }
+        if (lane == 0) { tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); }
         EntryFeed f;
         int k_issued = 0, v_issued = 0;
         for (int j = 0; j < E; ++j) {
@@ -189,18 +221,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 mbar_wait(k_full(d % kKStages), (d / kKStages) & 1, nullptr, p.status);
             for (int d = (v_issued > kVStages ? v_issued - kVStages : 0); d < v_issued; ++d)
                 mbar_wait(v_full(d % kVStages), (d / kVStages) & 1, nullptr, p.status);
-            mbar_wait(q_full, 0, nullptr, p.status);
         }
     } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            // S_w = Q K_w^T and dP_w = dO V_w^T for key rows [64w, 64w + 64) of stage s
+            // S_w = Q K_w^T and dP_w = dO V_w^T for key rows [64w, 64w + 64)
             auto issue_sdp = [&](int w, int ks, int vs) {
-                issue_qk<D>(tmem + col_s(w), sQ, sK + ks * L::kTile + w * 8192, idesc_s);
-                issue_qk<D>(tmem + col_dp(w), sDO, sV + vs * L::kTile + w * 8192, idesc_s);
+                issue_tk<D>(tmem + col_s(w), tmem + cQ, sK + ks * L::kTile + w * 8192, idesc_s);
+                issue_tk<D>(tmem + col_dp(w), tmem + cDO, sV + vs * L::kTile + w * 8192, idesc_s);
             };
-            bool ok = E > 0 && mbar_wait(q_full, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status) &&
+            bool ok = E > 0 && mbar_wait(qd_ready, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status) &&
                       mbar_wait(v_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
@@ -244,6 +275,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const int r_abs = q_row0 + rl, h = g * p.G + hl;
         const bool valid = rl < n_rows;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        // group 0 puts this lane's Q row into TMEM, group 1 its dO row
+        row_to_tmem<D>(tmem + lane_off + (w == 0 ? cQ : cDO),
+                       (w == 0 ? p.q : p.d_o) + (static_cast<size_t>(r_abs) * p.Hq + h) * D, valid);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(qd_ready);
         const float sl2 = p.scale_log2;
         const float lse2 = valid ? __ldg(p.lse + static_cast<size_t>(h) * p.N + r_abs) * kLog2e : INFINITY;
         const float delta = valid ? p.delta[static_cast<size_t>(h) * p.N + r_abs] : 0.f;
@@ -253,8 +290,6 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
             ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
-            const int j0 = e.x * kTileRows + 64 * w;
-            const int hi = (e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z;
             uint32_t sv[2][32], dpv[2][32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -262,22 +297,39 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_ld32(tmem + lane_off + col_dp(w) + 32 * c, dpv[c]);
             }
             tmem_wait_ld();                          // one TMEM round trip per half
+            if (e.w == 0) {                          // whole tile visible: no masks
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t ds[16];
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ds[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float pr[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int jj = j0 + 32 * c + 2 * i + u;
-                        const float pv = ex2(fmaf(__uint_as_float(sv[c][2 * i + u]), sl2, -lse2));
-                        const bool vis = e.w == 0 || (jj >= e.y && jj < hi);
-                        pr[u] = vis ? pv * (__uint_as_float(dpv[c][2 * i + u]) - delta) : 0.f;
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -lse2));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -lse2));
+                        ds[i] = pack_bf16(p0 * (__uint_as_float(dpv[c][2 * i]) - delta),
+                                          p1 * (__uint_as_float(dpv[c][2 * i + 1]) - delta));
                     }
-                    ds[i] = pack_bf16(pr[0], pr[1]);
+                    tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, ds);
                 }
-                tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, ds);
+            } else {
+                const int j0 = e.x * kTileRows + 64 * w;
+                const int lo = e.y - j0;
+                const int hi = ((e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z) - j0;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ds[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float pr[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int jj = 32 * c + 2 * i + u;
+                            const float pv = ex2(fmaf(__uint_as_float(sv[c][2 * i + u]), sl2, -lse2));
+                            pr[u] = (jj >= lo && jj < hi) ? pv * (__uint_as_float(dpv[c][2 * i + u]) - delta) : 0.f;
+                        }
+                        ds[i] = pack_bf16(pr[0], pr[1]);
+                    }
+                    tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, ds);
+                }
             }
             tmem_wait_st();
             tc_fence_before();

@@ -145,21 +145,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, kTileRows, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
+            // descriptors are built once per tile; stepping along K only moves the 14-bit
+            // start-address field, so each step is a 64-bit add of a compile-time constant
             auto issue_s = [&](int t, int ks) {
+                const uint64_t a0 = sdesc_sw128(sQ + t * L::kQTile, 16, 1024);
+                const uint64_t b0 = sdesc_sw128(sK + ks * L::kKV, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + t * L::kQTile + koff, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sK + ks * L::kKV + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + t * 128, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint64_t koff = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + t * 128, a0 + koff, b0 + koff, idesc_s, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int vs, bool acc) {
+                const uint64_t b0 = sdesc_sw128(sV + vs * L::kKV, kTileRows * 128, 1024);
 #pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(sV + vs * L::kKV + kk * 16 * 128, kTileRows * 128, 1024);
-                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                           idesc_o, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = E > 0 && mbar_wait(q_full, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status);
             if (ok) {

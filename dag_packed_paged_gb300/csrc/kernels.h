@@ -42,6 +42,7 @@ struct BwdParams {
     int32_t Hq, Hkv, G, R;
     float scale;                // softmax scale
     float scale_log2;
+    const __nv_bfloat16 *q;     // [N, Hq, D]
     const __nv_bfloat16 *o;     // [N, Hq, D]
     const __nv_bfloat16 *d_o;   // [N, Hq, D]
     const float *lse;           // [Hq, N]
