@@ -361,6 +361,8 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.scale = h.scale;
     p.scale_log2 = h.scale * 1.4426950408889634f;
     p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<const __nv_bfloat16 *>(v_pool);
     p.o = static_cast<const __nv_bfloat16 *>(o);
     p.d_o = static_cast<const __nv_bfloat16 *>(d_o);
     p.lse = lse;

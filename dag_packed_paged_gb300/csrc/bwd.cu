@@ -285,8 +285,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const float lse2 = valid ? __ldg(p.lse + static_cast<size_t>(h) * p.N + r_abs) * kLog2e : INFINITY;
         const float delta = valid ? p.delta[static_cast<size_t>(h) * p.N + r_abs] : 0.f;
         bool ok = true;
+        WarpRecords recs;
         for (int j = 0; j < E; ++j) {
-            const int4 e = __ldg(&entries[j]);
+            const int4 e = recs.get(entries, j, E, lane);
             ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
@@ -539,9 +540,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int jj = tile * kTileRows + row;          // its compact row
         const float sl2 = p.scale_log2;
         bool ok = true;
+        WarpRecords recs;
         for (int u = 0; u < U; ++u) {
             const int s = u % kStages;
-            const int4 te = __ldg(&tinfo[u >> 1]);
+            const int4 te = recs.get(tinfo, u >> 1, n_ent, lane);
             ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), u & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();

@@ -209,8 +209,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        WarpRecords recs;
         for (int j = 0; j < E; ++j) {
-            const int4 e = __ldg(&entries[j]);
+            const int4 e = recs.get(entries, j, E, lane);
             ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, abort, p.status));
             if (!ok) break;                          // warp-uniform: tcgen05.ld/st are collective
             tc_fence_after();
@@ -245,13 +246,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     m_used = m_new;
                 }
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tO + c * 32, v);
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(tO + c * 16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                    tmem_st32(tO + c * 32, v);
+                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                    tmem_st16(tO + c * 16, v);
                 }
                 tmem_wait_st();
             }

@@ -43,6 +43,8 @@ struct BwdParams {
     float scale;                // softmax scale
     float scale_log2;
     const __nv_bfloat16 *q;     // [N, Hq, D]
+    const __nv_bfloat16 *k_pool;  // [num_pages, P, Hkv, D]
+    const __nv_bfloat16 *v_pool;
     const __nv_bfloat16 *o;     // [N, Hq, D]
     const __nv_bfloat16 *d_o;   // [N, Hq, D]
     const float *lse;           // [Hq, N]
