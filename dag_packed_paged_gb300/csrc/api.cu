@@ -118,8 +118,8 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     if (pos_ids_out && h.N > 0) std::memcpy(pos_ids_out, h.pos_ids.data(), sizeof(int32_t) * h.N);
     {
         const ta_config &c = h.cfg;
-        plan->ws_delta_bytes = align_up(sizeof(float) * size_t(c.num_q_heads) * size_t(h.N), 256);
-        plan->ws_bytes = plan->ws_delta_bytes +
+        plan->ws_table_bytes = align_up(sizeof(float) * 256 * 2 * size_t(c.num_kv_heads) * (h.blocks.size() / 4), 256);
+        plan->ws_bytes = plan->ws_table_bytes +
                          sizeof(float) * size_t(h.n_partial_slots) * c.num_kv_heads * 2 * kTileRows * c.head_dim;
     }
     if (h.cfg.flags & TA_PLAN_HOST_ONLY) {
@@ -366,8 +366,9 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.o = static_cast<const __nv_bfloat16 *>(o);
     p.d_o = static_cast<const __nv_bfloat16 *>(d_o);
     p.lse = lse;
-    p.delta = static_cast<float *>(workspace);
-    p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan->ws_delta_bytes);
+    p.utab = static_cast<float *>(workspace);
+    p.n_blocks = int32_t(h.blocks.size() / 4);
+    p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan->ws_table_bytes);
     p.dq = dq;
     p.dk_pool = dk_pool;
     p.dv_pool = dv_pool;

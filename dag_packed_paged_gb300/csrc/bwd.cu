@@ -26,22 +26,41 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------------------ delta
+// One CTA per (query block, KV head, 128-lane query tile); thread m handles query lane m,
+// i.e. row (head hl, row rl) with 128 t + m = hl R + rl.  It writes the tile's 1 KB unit
+// table: [m] = lse * log2(e) (+inf for padding lanes, so that P = 0 there) and
+// [128 + m] = delta = <dO, O> of that row.  Both backward kernels read these per-lane
+// values from the table; the dK/dV loader copies a whole tile's table with one bulk copy.
 template <int D>
-__global__ void __launch_bounds__(256) delta_kernel(const BwdParams p) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int total = p.N * p.Hq;
-    if (warp >= total) return;
-    const int r = warp / p.Hq, h = warp % p.Hq;
-    const size_t base = (static_cast<size_t>(r) * p.Hq + h) * D;
-    float acc = 0.f;
-    constexpr int V = D / 32;   // elements per lane
-    const __nv_bfloat16 *a = p.d_o + base + lane * V;
-    const __nv_bfloat16 *b = p.o + base + lane * V;
+__global__ void __launch_bounds__(128) delta_kernel(const BwdParams p) {
+    const int t = blockIdx.x & 1, g = (blockIdx.x >> 1) % p.Hkv, qb = (blockIdx.x >> 1) / p.Hkv;
+    const int m = threadIdx.x, m_flat = 128 * t + m;
+    const int hl = m_flat / p.R, rl = m_flat % p.R, h = g * p.G + hl;
+    const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
+    const bool valid = rl < n_rows;
+    float lse2 = INFINITY, acc = 0.f;
+    if (valid) {
+        const int r = q_row0 + rl;
+        const size_t base = (static_cast<size_t>(r) * p.Hq + h) * D;
+        const uint4 *a = reinterpret_cast<const uint4 *>(p.d_o + base);
+        const uint4 *b = reinterpret_cast<const uint4 *>(p.o + base);
 #pragma unroll
-    for (int i = 0; i < V; ++i) acc += __bfloat162float(a[i]) * __bfloat162float(b[i]);
+        for (int i = 0; i < D / 8; ++i) {
+            const uint4 x = __ldg(a + i), y = __ldg(b + i);
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) p.delta[static_cast<size_t>(h) * p.N + r] = acc;
+            for (int k = 0; k < 4; ++k) {
+                const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xs[k]));
+                const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ys[k]));
+                acc = fmaf(fx.x, fy.x, acc);
+                acc = fmaf(fx.y, fy.y, acc);
+            }
+        }
+        lse2 = __ldg(p.lse + static_cast<size_t>(h) * p.N + r) * kLog2e;
+    }
+    float *tab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
+    tab[m] = lse2;
+    tab[128 + m] = acc;
 }
 
 // One 128-lane query tile t of a block: rows (head, row) flattened as m = hl * R + rl.
@@ -282,8 +301,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         tc_fence_before();
         mbar_arrive(qd_ready);
         const float sl2 = p.scale_log2;
-        const float lse2 = valid ? __ldg(p.lse + static_cast<size_t>(h) * p.N + r_abs) * kLog2e : INFINITY;
-        const float delta = valid ? p.delta[static_cast<size_t>(h) * p.N + r_abs] : 0.f;
+        const float *tab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
+        const float lse2 = tab[32 * q4 + lane];
+        const float delta = tab[128 + 32 * q4 + lane];
         bool ok = true;
         WarpRecords recs;
         for (int j = 0; j < E; ++j) {
@@ -371,17 +391,24 @@ struct DkvLayout {
     static constexpr int k_off = 0;
     static constexpr int v_off = k_off + kTile;
     static constexpr int q_off = v_off + kTile;                 // stage s: Q at q_off + s*2*kTile, dO after it
-    static constexpr int lse_off = q_off + kStages * 2 * kTile; // stage s: 128 lse2 + 128 delta + 128 rows
-    static constexpr int bar_off = lse_off + kStages * 3 * 128 * 4;
-    static constexpr int n_bars = 1 + 2 * kStages + 2 + 2 + 1;
+    static constexpr int lse_off = q_off + kStages * 2 * kTile; // stage s: the unit table (128 lse2 + 128 delta)
+    static constexpr int bar_off = lse_off + kStages * 256 * 4;
+    static constexpr int n_bars = 1 + 2 * kStages + 4 + 1;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;
 };
 
 // One CTA = one key tile x one KV head x one chunk of the tile's readers.  K and V stay in
-// shared memory; for every (reader block, 128-lane query tile): S^T_w = K Q_w^T and
-// dP^T_w = V dO_w^T for the two 64-lane halves w of the query tile, P^T_w and dS^T_w back
-// into TMEM as bf16, then dV += P^T_w dO_w and dK += dS^T_w Q_w, accumulated in TMEM.
+// shared memory.  Every (reader block, 128-lane query tile) is one unit, processed in two
+// phases so that the tensor core always has work while the elementwise warps run:
+//   MMA:  S^T = K Q^T, dP^T = V dO^T                       (128 x 128 each, into TMEM)
+//   EW :  P^T = exp2(S^T log2e scale - lse) (masked), bf16 copy into TMEM      -> p_full
+//   MMA:  dV += P^T dO,  then the next unit's S^T             (while EW computes dS)
+//   EW :  dS^T = P^T (dP^T - delta), bf16 copy into TMEM                        -> ds_full
+//   MMA:  dK += dS^T Q,  then the next unit's dP^T            (while EW computes the next P)
+// The two elementwise warpgroups split each unit's 128 query columns (64 each); P stays in
+// their registers between the phases.  dV and dK accumulate in TMEM for the whole chunk and
+// each key row of the tile is written once at the end.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -395,19 +422,19 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int ci = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
     const int tile = __ldg(p.chunks + 4 * ci), a0 = __ldg(p.chunks + 4 * ci + 1);
     const int n_ent = __ldg(p.chunks + 4 * ci + 2) - a0, slot = __ldg(p.chunks + 4 * ci + 3);
-    const int4 *tinfo = reinterpret_cast<const int4 *>(p.t_info) + a0;   // first row, rows<<8|flags, lo, hi
+    const int4 *tinfo = reinterpret_cast<const int4 *>(p.t_info) + a0;   // block<<2|flags, first row, lo, hi
     const int U = 2 * n_ent;   // (entry, query tile) units
 
     const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off;
     auto sQ = [&](int s) { return sbase + L::q_off + s * 2 * L::kTile; };
     auto sDO = [&](int s) { return sbase + L::q_off + s * 2 * L::kTile + L::kTile; };
-    float *lse_s = reinterpret_cast<float *>(smem + L::lse_off);     // [stage][3][128]
+    float *lse_s = reinterpret_cast<float *>(smem + L::lse_off);     // [stage][256]
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
     const uint32_t kv_full = bar(0);
     auto qd_full = [&](int s) { return bar(1 + s); };
     auto qd_empty = [&](int s) { return bar(1 + kStages + s); };
-    auto s_full = [&](int w) { return bar(1 + 2 * kStages + w); };
-    auto p_full = [&](int w) { return bar(3 + 2 * kStages + w); };
+    const uint32_t s_full = bar(1 + 2 * kStages), dp_full = bar(2 + 2 * kStages);
+    const uint32_t p_full = bar(3 + 2 * kStages), ds_full = bar(4 + 2 * kStages);
     const uint32_t o_full = bar(5 + 2 * kStages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
@@ -415,7 +442,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < kStages; ++s) { mbar_init(qd_full(s), 1); mbar_init(qd_empty(s), 1); }
-        for (int w = 0; w < 2; ++w) { mbar_init(s_full(w), 1); mbar_init(p_full(w), 128); }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_full, 256);
+        mbar_init(ds_full, 256);
         mbar_init(o_full, 1);
         *abort = 0;
         fence_barrier_init();
@@ -428,7 +458,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t cDV = 0, cDK = D;   // dV [0, D), dK [D, 2D)
+    // TMEM columns: S^T [0,128) | dP^T [128,256) | dV [256, 256+D) | dK [384, 384+D).
+    // Group w's bf16 P^T (query columns [64w, 64w+64)) goes to S^T columns [64w, 64w+32),
+    // its dS^T to dP^T columns [64w, 64w+32): inside its own half, so no group overwrites
+    // scores the other group has not read yet.
+    constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 384;
 
     if (warp == 8) {
         // ---------------------------------------------------------------- loads (whole warp)
@@ -443,40 +477,20 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tma_kv_tile(sK, &tm_k, ky, ppt, p.page_size, g, D, kv_full);
             tma_kv_tile(sV, &tm_v, ky, ppt, p.page_size, g, D, kv_full);
         }
-        const int log2R = 31 - __clz(p.R);
         int4 mine = make_int4(0, 0, 0, 0);   // lane i holds the reader info of entry (base + i)
         int issued = 0;
         for (int u = 0; u < U; ++u) {
             const int s = u % kStages, t = u & 1, e = u >> 1;
             if ((u & 63) == 0 && e + lane < n_ent) mine = __ldg(tinfo + e + lane);
-            const int q_row0 = __shfl_sync(0xffffffffu, mine.x, e & 31);
-            const int n_rows = __shfl_sync(0xffffffffu, mine.y, e & 31) >> 8;
-            // issue every lse / delta load before the first shared-memory store
-            float lv[4], dl[4];
-            int rr[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int m_flat = 128 * t + lane + 32 * i;
-                const int hl = m_flat >> log2R, rl = m_flat & (p.R - 1);
-                const size_t idx = static_cast<size_t>(g * p.G + hl) * p.N + q_row0 + rl;
-                const bool valid = rl < n_rows;
-                lv[i] = valid ? __ldg(p.lse + idx) * kLog2e : INFINITY;      // +inf: P = 0 for padding rows
-                dl[i] = valid ? __ldg(p.delta + idx) : 0.f;
-                rr[i] = q_row0 + rl;
-            }
+            const int qb = __shfl_sync(0xffffffffu, mine.x, e & 31) >> 2;
+            const int q_row0 = __shfl_sync(0xffffffffu, mine.y, e & 31);
             bool ok = true;
             if (lane == 0 && u >= kStages) ok = mbar_wait(qd_empty(s), ((u / kStages) - 1) & 1, abort, p.status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-            float *ls = lse_s + s * 3 * 128;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                ls[lane + 32 * i] = lv[i];
-                ls[128 + lane + 32 * i] = dl[i];
-                reinterpret_cast<int *>(ls)[256 + lane + 32 * i] = rr[i];
-            }
-            __syncwarp();
             if (lane == 0) {
-                mbar_arrive_expect_tx(qd_full(s), 2 * L::kTile);
+                mbar_arrive_expect_tx(qd_full(s), 2 * L::kTile + 1024);
+                bulk_load(smem_u32(lse_s + s * 256), p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256,
+                          1024, qd_full(s));
                 load_q_tile(sQ(s), &tm_q, t, g, p.G, p.R, D, q_row0, qd_full(s));
                 load_q_tile(sDO(s), &tm_do, t, g, p.G, p.R, D, q_row0, qd_full(s));
             }
@@ -489,44 +503,42 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
     } else if (warp == 9) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            // S^T_w = K Q_w^T, dP^T_w = V dO_w^T for query lanes [64w, 64w + 64) of stage s
-            auto issue_sdp = [&](int w, int s) {
-                issue_qk<D>(tmem + col_s(w), sK, sQ(s) + w * 8192, idesc_s);
-                issue_qk<D>(tmem + col_dp(w), sV, sDO(s) + w * 8192, idesc_s);
-            };
-            // dV += P^T_w dO_w, dK += dS^T_w Q_w (64 query lanes of stage s)
-            auto issue_acc = [&](int w, int s, bool acc) {
-                issue_tn_k<D, 64>(tmem + cDV, tmem + col_s(w), sDO(s) + w * 8192, idesc_o, acc);
-                issue_tn_k<D, 64>(tmem + cDK, tmem + col_dp(w), sQ(s) + w * 8192, idesc_o, acc);
+            // D[128 x D] += A^T-part in TMEM (query columns split as above) * B rows of stage s
+            auto issue_acc = [&](uint32_t d_tmem, uint32_t a_base, uint32_t sB, bool acc) {
+                const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                    mma_ts(d_tmem, a_base + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                           b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(qd_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0);
-                mma_commit(s_full(0));
-                issue_sdp(1, 0);
-                mma_commit(s_full(1));
+                issue_qk<D>(tmem + cS, sK, sQ(0), idesc_s);        // S^T = K Q^T
+                mma_commit(s_full);
+                issue_qk<D>(tmem + cDP, sV, sDO(0), idesc_s);      // dP^T = V dO^T
+                mma_commit(dp_full);
             }
             for (int u = 0; ok && u < U; ++u) {
                 const int s = u % kStages, s1 = (u + 1) % kStages;
-                if (!(ok = mbar_wait(p_full(0), u & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc(0, s, u > 0);
+                issue_acc(tmem + cDV, tmem + cS, sDO(s), u > 0);    // dV += P^T dO
                 if (u + 1 < U) {
                     if (!(ok = mbar_wait(qd_full(s1), ((u + 1) / kStages) & 1, abort, p.status))) break;
                     tc_fence_after();
-                    issue_sdp(0, s1);
-                    mma_commit(s_full(0));
+                    issue_qk<D>(tmem + cS, sK, sQ(s1), idesc_s);
+                    mma_commit(s_full);
                 }
-                if (!(ok = mbar_wait(p_full(1), u & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(ds_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc(1, s, true);
+                issue_acc(tmem + cDK, tmem + cDP, sQ(s), u > 0);    // dK += dS^T Q
                 mma_commit(qd_empty(s));
                 if (u + 1 < U) {
-                    issue_sdp(1, s1);
-                    mma_commit(s_full(1));
+                    issue_qk<D>(tmem + cDP, sV, sDO(s1), idesc_s);
+                    mma_commit(dp_full);
                 }
             }
             mma_commit(o_full);
@@ -544,43 +556,81 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         for (int u = 0; u < U; ++u) {
             const int s = u % kStages;
             const int4 te = recs.get(tinfo, u >> 1, n_ent, lane);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), u & 1, abort, p.status));
+            // s_full implies the stage was loaded; waiting on qd_full as well makes the bulk-copied
+            // table visible to this thread directly
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, abort, p.status) &&
+                                             mbar_wait(qd_full(s), (u / kStages) & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
-            const float *ls = lse_s + s * 3 * 128 + 64 * w;
-            const int *rs = reinterpret_cast<const int *>(lse_s + s * 3 * 128) + 256 + 64 * w;
+            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + s * 256 + 64 * w);
+            const float4 *dl4 = reinterpret_cast<const float4 *>(lse_s + s * 256 + 128 + 64 * w);
             const bool row_in = jj >= te.z && jj < te.w;
-            const bool causal = (te.y & kEntryCausal) != 0;
-            uint32_t sv[2][32], dpv[2][32];
+            const bool causal = (te.x & kEntryCausal) != 0;
+            // query row of lane m of this group's columns: first row + ((128 t + 64 w + m) mod R)
+            const int rbase = te.y, rmask = p.R - 1, mbase = 128 * (u & 1) + 64 * w;
+            // ---------------- phase 1: P^T
+            float pf[64];
+            {
+                uint32_t sv[2][32];
+                tmem_ld32(tmem + lane_off + cS + 64 * w, sv[0]);
+                tmem_ld32(tmem + lane_off + cS + 64 * w + 32, sv[1]);
+                tmem_wait_ld();
+                if (!row_in) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(tmem + lane_off + col_s(w) + 32 * c, sv[c]);
-                tmem_ld32(tmem + lane_off + col_dp(w) + 32 * c, dpv[c]);
-            }
-            tmem_wait_ld();                          // one TMEM round trip per half
+                    for (int i = 0; i < 64; ++i) pf[i] = 0.f;
+                } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[16], dk[16];
+                    for (int i4 = 0; i4 < 16; ++i4) {
+                        const float4 l4 = ls4[i4];
+                        const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float pr[2], dr[2];
+                        for (int v = 0; v < 4; ++v)
+                            pf[4 * i4 + v] = ex2(fmaf(__uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + v]), sl2, -lq[v]));
+                        if (causal) {
 #pragma unroll
-                    for (int v = 0; v < 2; ++v) {
-                        const int m = 32 * c + 2 * i + v;
-                        float pv = ex2(fmaf(__uint_as_float(sv[c][2 * i + v]), sl2, -ls[m]));
-                        if (!row_in || (causal && jj > rs[m])) pv = 0.f;
-                        pr[v] = pv;
-                        dr[v] = pv * (__uint_as_float(dpv[c][2 * i + v]) - ls[128 + m]);
+                            for (int v = 0; v < 4; ++v) {
+                                const int r = rbase + ((mbase + 4 * i4 + v) & rmask);
+                                pf[4 * i4 + v] = jj > r ? 0.f : pf[4 * i4 + v];
+                            }
+                        }
                     }
-                    pk[i] = pack_bf16(pr[0], pr[1]);
-                    dk[i] = pack_bf16(dr[0], dr[1]);
                 }
-                tmem_st16(tmem + lane_off + col_s(w) + 16 * c, pk);
-                tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, dk);
+                uint32_t pk[2][16];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i >> 4][i & 15] = pack_bf16(pf[2 * i], pf[2 * i + 1]);
+                tmem_st16(tmem + lane_off + cS + 64 * w, pk[0]);
+                tmem_st16(tmem + lane_off + cS + 64 * w + 16, pk[1]);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(p_full(w));
+            // ---------------- phase 2: dS^T
+            ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, abort, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                uint32_t dv[2][32];
+                tmem_ld32(tmem + lane_off + cDP + 64 * w, dv[0]);
+                tmem_ld32(tmem + lane_off + cDP + 64 * w + 32, dv[1]);
+                tmem_wait_ld();
+                uint32_t dk[2][16];
+#pragma unroll
+                for (int i4 = 0; i4 < 16; ++i4) {
+                    const float4 d4 = dl4[i4];
+                    const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float dr[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dr[v] = pf[4 * i4 + v] * (__uint_as_float(dv[i4 >> 3][4 * (i4 & 7) + v]) - dq4[v]);
+                    dk[i4 >> 3][2 * (i4 & 7)] = pack_bf16(dr[0], dr[1]);
+                    dk[i4 >> 3][2 * (i4 & 7) + 1] = pack_bf16(dr[2], dr[3]);
+                }
+                tmem_st16(tmem + lane_off + cDP + 64 * w, dk[0]);
+                tmem_st16(tmem + lane_off + cDP + 64 * w + 16, dk[1]);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(ds_full);
+            }
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
@@ -651,9 +701,8 @@ template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                          const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
                          cudaStream_t stream, void *const *trace) {
-    const long long rows = static_cast<long long>(p.N) * p.Hq;
     trace_record(trace, 2, stream);
-    delta_kernel<D><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p);
+    delta_kernel<D><<<static_cast<unsigned>(n_blocks) * p.Hkv * 2, 128, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::bytes);

@@ -34,7 +34,7 @@ struct BwdParams {
     const int32_t *order;
     const int32_t *page_table;
     const int32_t *tile_rows;
-    const int32_t *t_info;      // per tile-major entry: first row, rows << 8 | flags, lo, hi
+    const int32_t *t_info;      // per tile-major entry: block << 2 | flags, first row, lo, hi
     int32_t n_logical_pages;
     int32_t num_pages;
     int32_t page_size;
@@ -48,7 +48,8 @@ struct BwdParams {
     const __nv_bfloat16 *o;     // [N, Hq, D]
     const __nv_bfloat16 *d_o;   // [N, Hq, D]
     const float *lse;           // [Hq, N]
-    float *delta;               // [Hq, N] (workspace)
+    float *utab;                // [Hkv][n_blocks][2 query tiles][128 lse*log2e | 128 delta] (workspace)
+    int32_t n_blocks;
     float *dq;                  // [N, Hq, D]
     float *dk_pool;             // [num_pages, P, Hkv, D]
     float *dv_pool;

@@ -5,8 +5,9 @@
 // (there is no hook to request scratch), and latency-critical loops that forbid device
 // allocation once they are running, because cudaMalloc can synchronise the device and a
 // fresh allocation may fail or fragment a carefully sized pool.  For them the backward's
-// scratch -- delta [Hq, N] fp32 and the dK/dV partial slots of key tiles whose readers
-// were split -- lives in one fixed array inside this library instead.
+// scratch -- a small table of lse and delta values per query tile and the dK/dV partial
+// slots of key tiles whose readers were split -- lives in one fixed array inside this
+// library instead.
 //
 // The array below is a file-scope __device__ variable: every GPU that loads the library
 // holds all of it until the process exits.  In host code its name is only a host-side

@@ -400,8 +400,8 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
         P.t_info.assign(4 * n_entries, 0);
         for (int64_t e = 0; e < n_entries; ++e) {
             const int32_t b = P.t_entries[4 * e];
-            P.t_info[4 * e] = blocks[4 * b];
-            P.t_info[4 * e + 1] = (blocks[4 * b + 1] << 8) | P.t_entries[4 * e + 3];
+            P.t_info[4 * e] = (b << 2) | P.t_entries[4 * e + 3];
+            P.t_info[4 * e + 1] = blocks[4 * b];
             P.t_info[4 * e + 2] = P.t_entries[4 * e + 1];
             P.t_info[4 * e + 3] = P.t_entries[4 * e + 2];
         }

@@ -38,7 +38,7 @@ struct HostPlan {
     std::vector<int32_t> page_table;
     std::vector<int32_t> tile_rows;   // per key tile, per page: TMA row of the page in the pool
                                       // (pool rows; num_pages * P past the strip: zero fill)
-    std::vector<int32_t> t_info;      // per tile-major entry: first row, rows << 8 | flags, lo, hi
+    std::vector<int32_t> t_info;      // per tile-major entry: block << 2 | flags, first row, lo, hi
     int64_t n_segments = 0;
     int64_t n_partial_slots = 0;
     int64_t pairs = 0;
@@ -67,7 +67,7 @@ struct ta_plan {
     const int32_t *d_tile_rows = nullptr;
     const int32_t *d_t_info = nullptr;
     int32_t *d_status = nullptr;      // bounded-wait status words (zeroed at plan time)
-    size_t ws_delta_bytes = 0;        // workspace: delta [Hq, N] fp32, 256-aligned
+    size_t ws_table_bytes = 0;        // workspace: per (KV head, block, query tile) 128 lse*log2e + 128 delta
     size_t ws_bytes = 0;              // total bwd workspace
     int device = 0;
     int num_sms = 0;

@@ -218,7 +218,8 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
  * no counterpart to this; it exists for callers that cannot give the library device scratch:
  * plugin-style hosts that pass a kernel only its input and output buffers, and loops that
  * forbid device allocation while running (cudaMalloc can synchronise the device and may fail
- * or fragment a sized pool).  It allocates nothing.  The scratch (delta and dK/dV partials)
+ * or fragment a sized pool).  It allocates nothing.  The scratch (the lse/delta table and dK/dV
+ * partials)
  * is a fixed 64 MiB array inside the library that every GPU loading the library holds until
  * the process exits; plans needing more (tree_attn_bwd_workspace_size(plan) > 64 MiB) are
  * rejected with TA_ERR_UNSUPPORTED and a message naming the size.  The first call on a device
@@ -232,7 +233,8 @@ int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const void *k_pool
                           const void *o, const float *lse, const void *d_o, float *dq, float *dk_pool,
                           float *dv_pool, void *stream);
 
-/* Bytes of device scratch tree_attn_bwd needs for this plan (delta and dK/dV partials). */
+/* Bytes of device scratch tree_attn_bwd needs for this plan: a 1 KB table per (KV head, query
+ * block, 128-lane query tile) holding lse * log2(e) and delta, plus dK/dV partial slots. */
 size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
 
 /* Synchronises `stream` and reports whether any bounded device wait of this plan's kernels
