@@ -7,7 +7,8 @@
 // "differentiable mount edges", HARTS arXiv 2608.28158 Section 3.4 gather backward).
 //
 // Four launches:
-//   delta_kernel   delta[h, r] = <dO[r,h], O[r,h]>                           (HBM-bound)
+//   delta_kernel   per (query block, KV head, 128-lane query tile): each lane's lse * log2(e)
+//                  and delta = <dO, O>, one 1 KB table per tile                (HBM-bound)
 //   dq_kernel      query-major: one CTA per (query block, KV head, 128-lane query tile);
 //                  walks the block's key-tile entries like the forward
 //   dkdv_kernel    key-major: one CTA per (key-tile chunk, KV head); walks the query blocks
@@ -86,27 +87,10 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t 
     }
 }
 
-template <int D, int KROWS>
-__device__ __forceinline__ void issue_tn_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc, bool acc) {
-    // D[128 x D] (+)= A[128 x KROWS] (bf16 in TMEM) * B[KROWS x D] (rows of an MN-major tile)
-    const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
-#pragma unroll
-    for (int kk = 0; kk < KROWS / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
-               (acc || kk > 0) ? 1u : 0u);
-}
-
-// Both backward kernels split every 128-column S / dP tile into two 64-column halves,
-// double-buffered in TMEM, each half owned by one elementwise warpgroup: while one group
-// turns its half of S and dP into P / dS, the tensor core runs the other half's
-// accumulations and the next half's S and dP.
-constexpr int kBwdThreads = 320;   // warps 0-3 half a, 4-7 half b, 8 loads, 9 MMA
+constexpr int kBwdThreads = 320;   // warps 0-3 / 4-7: elementwise groups, 8 loads, 9 MMA
 constexpr int kStages = 2;         // dK/dV: Q/dO stages
 constexpr int kKStages = 3;        // dQ: K stages (K is held until the dQ MMAs)
 constexpr int kVStages = 3;        // dQ: V stages (V is released after the dP MMAs)
-// TMEM columns of the two half buffers: S_w [256+128w, 320+128w), dP_w [320+128w, 384+128w)
-__host__ __device__ constexpr uint32_t col_s(int w) { return 256u + 128u * w; }
-__host__ __device__ constexpr uint32_t col_dp(int w) { return 320u + 128u * w; }
 
 template <int D>
 __device__ __forceinline__ void issue_tk(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB, uint32_t idesc) {
@@ -118,6 +102,18 @@ __device__ __forceinline__ void issue_tk(uint32_t d_tmem, uint32_t a_tmem, uint3
         mma_ts(d_tmem, a_tmem + kk * 8,
                b0 + static_cast<uint64_t>(((kk >> 2) * (kTileRows * 128) + (kk & 3) * 32) >> 4), idesc,
                kk > 0 ? 1u : 0u);
+}
+
+// D[128 x N] (+)= A[128 x 128] * B[128 x N], A in bf16 TMEM columns written by the two
+// elementwise groups (group w's 64 K-columns packed into columns [64w, 64w + 32) of a_base),
+// B the rows of an MN-major smem tile (N = D contiguous, LBO = one 64-column half).
+__device__ __forceinline__ void issue_acc_split(uint32_t d_tmem, uint32_t a_base, uint32_t sB, uint32_t idesc,
+                                                bool acc) {
+    const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
+#pragma unroll
+    for (int kk = 0; kk < kTileRows / 16; ++kk)
+        mma_ts(d_tmem, a_base + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+               b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
 // Copy one bf16 row of D elements from global memory into this thread's TMEM lane at
@@ -149,15 +145,21 @@ struct DqLayout {
     static constexpr int k_off = 0;
     static constexpr int v_off = k_off + kKStages * kTile;
     static constexpr int bar_off = v_off + kVStages * kTile;
-    static constexpr int n_bars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1;
+    static constexpr int n_bars = 1 + 2 * kKStages + 2 * kVStages + 5;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;
 };
 
 // One CTA = one 128-lane query tile (t) of one query block x one KV head.  The tile's Q and
 // dO rows stay in TMEM for the CTA's lifetime, so S = Q K^T and dP = dO V^T read only the
-// key tile from shared memory.  Per key-tile entry: S_w, dP_w for the two 64-row halves w of
-// the key tile, dS_w = P_w (dP_w - delta) back into TMEM as bf16, then dQ += dS_w K_w.
+// key tile from shared memory.  Per key-tile entry j, with full-width (N = 128) MMAs:
+//   MMA:  S_j = Q K_j^T, dP_j = dO V_j^T                        (into TMEM)
+//   EW :  read S_j (frees it: S_{j+1} starts), P_j = exp2(S_j scale log2e - lse) masked
+//   EW :  dS_j = P_j (dP_j - delta), bf16 into the dP columns                  -> ds_full
+//   MMA:  dQ += dS_j K_j, then dP_{j+1}
+// The two elementwise groups split each entry's 128 key columns (64 each); P stays in their
+// registers between the phases.  The chain that sets the pace is dQ_j -> dP_{j+1} -> dS_{j+1};
+// S_{j+1} runs on the tensor core while the groups compute dS_j.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -181,9 +183,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     auto k_empty = [&](int s) { return bar(1 + kKStages + s); };
     auto v_full = [&](int s) { return bar(1 + 2 * kKStages + s); };
     auto v_empty = [&](int s) { return bar(1 + 2 * kKStages + kVStages + s); };
-    auto s_full = [&](int w) { return bar(1 + 2 * kKStages + 2 * kVStages + w); };
-    auto p_full = [&](int w) { return bar(3 + 2 * kKStages + 2 * kVStages + w); };
-    const uint32_t o_full = bar(5 + 2 * kKStages + 2 * kVStages);
+    constexpr int kb = 1 + 2 * kKStages + 2 * kVStages;
+    const uint32_t s_full = bar(kb), s_free = bar(kb + 1), dp_full = bar(kb + 2), ds_full = bar(kb + 3);
+    const uint32_t o_full = bar(kb + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
@@ -191,7 +193,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         mbar_init(qd_ready, 256);
         for (int s = 0; s < kKStages; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
-        for (int w = 0; w < 2; ++w) { mbar_init(s_full(w), 1); mbar_init(p_full(w), 128); }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 256);
+        mbar_init(dp_full, 1);
+        mbar_init(ds_full, 256);
         mbar_init(o_full, 1);
         *abort = 0;
         fence_barrier_init();
@@ -205,8 +210,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // TMEM columns: Q [0, D/2) and dO [64, 64 + D/2) as bf16 pairs, dQ [128, 128 + D),
-    // then the two S / dP half buffers
-    constexpr uint32_t cQ = 0, cDO = 64, cDQ = 128;
+    // S [256, 384), dP [384, 512); group w's dS goes to dP columns [384 + 64w, 384 + 64w + 32),
+    // inside the half it has already read.
+    constexpr uint32_t cQ = 0, cDO = 64, cDQ = 128, cS = 256, cDP = 384;
 
     if (warp == 8) {
         const int ppt = kTileRows / p.page_size;
@@ -243,43 +249,38 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         }
     } else if (warp == 9) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16(128, 64, 0, 0);
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            // S_w = Q K_w^T and dP_w = dO V_w^T for key rows [64w, 64w + 64)
-            auto issue_sdp = [&](int w, int ks, int vs) {
-                issue_tk<D>(tmem + col_s(w), tmem + cQ, sK + ks * L::kTile + w * 8192, idesc_s);
-                issue_tk<D>(tmem + col_dp(w), tmem + cDO, sV + vs * L::kTile + w * 8192, idesc_s);
-            };
             bool ok = E > 0 && mbar_wait(qd_ready, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status) &&
                       mbar_wait(v_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0, 0);
-                mma_commit(s_full(0));
-                issue_sdp(1, 0, 0);
-                mma_commit(s_full(1));
+                issue_tk<D>(tmem + cS, tmem + cQ, sK, idesc_s);        // S_0 = Q K_0^T
+                mma_commit(s_full);
+                issue_tk<D>(tmem + cDP, tmem + cDO, sV, idesc_s);      // dP_0 = dO V_0^T
+                mma_commit(dp_full);
                 mma_commit(v_empty(0));
             }
             for (int j = 0; ok && j < E; ++j) {
                 const int ks = j % kKStages, ks1 = (j + 1) % kKStages, vs1 = (j + 1) % kVStages;
-                if (!(ok = mbar_wait(p_full(0), j & 1, abort, p.status))) break;
-                tc_fence_after();
-                issue_tn_k<D, 64>(tmem + cDQ, tmem + col_dp(0), sK + ks * L::kTile, idesc_o, j > 0);
                 if (j + 1 < E) {
-                    if (!(ok = mbar_wait(k_full(ks1), ((j + 1) / kKStages) & 1, abort, p.status) &&
-                               mbar_wait(v_full(vs1), ((j + 1) / kVStages) & 1, abort, p.status)))
+                    // S_{j+1} as soon as both groups have read S_j
+                    if (!(ok = mbar_wait(s_free, j & 1, abort, p.status) &&
+                               mbar_wait(k_full(ks1), ((j + 1) / kKStages) & 1, abort, p.status)))
                         break;
                     tc_fence_after();
-                    issue_sdp(0, ks1, vs1);
-                    mma_commit(s_full(0));
+                    issue_tk<D>(tmem + cS, tmem + cQ, sK + ks1 * L::kTile, idesc_s);
+                    mma_commit(s_full);
                 }
-                if (!(ok = mbar_wait(p_full(1), j & 1, abort, p.status))) break;
+                if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_tn_k<D, 64>(tmem + cDQ, tmem + col_dp(1), sK + ks * L::kTile + 64 * 128, idesc_o, true);
+                issue_acc_split(tmem + cDQ, tmem + cDP, sK + ks * L::kTile, idesc_o, j > 0);   // dQ += dS_j K_j
                 mma_commit(k_empty(ks));
                 if (j + 1 < E) {
-                    issue_sdp(1, ks1, vs1);
-                    mma_commit(s_full(1));
+                    if (!(ok = mbar_wait(v_full(vs1), ((j + 1) / kVStages) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    issue_tk<D>(tmem + cDP, tmem + cDO, sV + vs1 * L::kTile, idesc_s);
+                    mma_commit(dp_full);
                     mma_commit(v_empty(vs1));
                 }
             }
@@ -308,53 +309,48 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         WarpRecords recs;
         for (int j = 0; j < E; ++j) {
             const int4 e = recs.get(entries, j, E, lane);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full(w), j & 1, abort, p.status));
+            // ---------------- phase 1: P_j from S_j
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sv[2][32], dpv[2][32];
+            float pf[64];
+            {
+                uint32_t sv[2][32];
+                tmem_ld32(tmem + lane_off + cS + 64 * w, sv[0]);
+                tmem_ld32(tmem + lane_off + cS + 64 * w + 32, sv[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(s_free);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(tmem + lane_off + col_s(w) + 32 * c, sv[c]);
-                tmem_ld32(tmem + lane_off + col_dp(w) + 32 * c, dpv[c]);
-            }
-            tmem_wait_ld();                          // one TMEM round trip per half
-            if (e.w == 0) {                          // whole tile visible: no masks
+                for (int i = 0; i < 64; ++i) pf[i] = ex2(fmaf(__uint_as_float(sv[i >> 5][i & 31]), sl2, -lse2));
+                if (e.w != 0) {                      // partial / diagonal tile: mask key columns
+                    const int j0 = e.x * kTileRows + 64 * w;
+                    const int lo = e.y - j0;
+                    const int hi = ((e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z) - j0;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t ds[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -lse2));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -lse2));
-                        ds[i] = pack_bf16(p0 * (__uint_as_float(dpv[c][2 * i]) - delta),
-                                          p1 * (__uint_as_float(dpv[c][2 * i + 1]) - delta));
-                    }
-                    tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, ds);
-                }
-            } else {
-                const int j0 = e.x * kTileRows + 64 * w;
-                const int lo = e.y - j0;
-                const int hi = ((e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z) - j0;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t ds[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float pr[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int jj = 32 * c + 2 * i + u;
-                            const float pv = ex2(fmaf(__uint_as_float(sv[c][2 * i + u]), sl2, -lse2));
-                            pr[u] = (jj >= lo && jj < hi) ? pv * (__uint_as_float(dpv[c][2 * i + u]) - delta) : 0.f;
-                        }
-                        ds[i] = pack_bf16(pr[0], pr[1]);
-                    }
-                    tmem_st16(tmem + lane_off + col_dp(w) + 16 * c, ds);
+                    for (int i = 0; i < 64; ++i) pf[i] = (i >= lo && i < hi) ? pf[i] : 0.f;
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(p_full(w));
+            // ---------------- phase 2: dS_j
+            ok = __all_sync(0xffffffffu, mbar_wait(dp_full, j & 1, abort, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                uint32_t dpv[2][32];
+                tmem_ld32(tmem + lane_off + cDP + 64 * w, dpv[0]);
+                tmem_ld32(tmem + lane_off + cDP + 64 * w + 32, dpv[1]);
+                tmem_wait_ld();
+                uint32_t ds[2][16];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    ds[i >> 4][i & 15] = pack_bf16(pf[2 * i] * (__uint_as_float(dpv[i >> 4][(2 * i) & 31]) - delta),
+                                                   pf[2 * i + 1] * (__uint_as_float(dpv[i >> 4][(2 * i + 1) & 31]) - delta));
+                tmem_st16(tmem + lane_off + cDP + 64 * w, ds[0]);
+                tmem_st16(tmem + lane_off + cDP + 64 * w + 16, ds[1]);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(ds_full);
+            }
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
@@ -505,14 +501,6 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            // D[128 x D] += A^T-part in TMEM (query columns split as above) * B rows of stage s
-            auto issue_acc = [&](uint32_t d_tmem, uint32_t a_base, uint32_t sB, bool acc) {
-                const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(d_tmem, a_base + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                           b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
-            };
             bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(qd_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
@@ -525,7 +513,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 const int s = u % kStages, s1 = (u + 1) % kStages;
                 if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc(tmem + cDV, tmem + cS, sDO(s), u > 0);    // dV += P^T dO
+                issue_acc_split(tmem + cDV, tmem + cS, sDO(s), idesc_o, u > 0);    // dV += P^T dO
                 if (u + 1 < U) {
                     if (!(ok = mbar_wait(qd_full(s1), ((u + 1) / kStages) & 1, abort, p.status))) break;
                     tc_fence_after();
@@ -534,7 +522,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 if (!(ok = mbar_wait(ds_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc(tmem + cDK, tmem + cDP, sQ(s), u > 0);    // dK += dS^T Q
+                issue_acc_split(tmem + cDK, tmem + cDP, sQ(s), idesc_o, u > 0);    // dK += dS^T Q
                 mma_commit(qd_empty(s));
                 if (u + 1 < U) {
                     issue_qk<D>(tmem + cDP, sV, sDO(s1), idesc_s);
