@@ -232,9 +232,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                     if (jj < e.y || jj >= hi) s[c] = -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            // row max: a tree of three-input maxima (16 independent chains, then a final fold)
+            float a16[16];
 #pragma unroll
-            for (int c = 0; c < kTileRows; ++c) mx = fmaxf(mx, s[c]);
+            for (int i = 0; i < 16; ++i) {
+                float m = max3(s[i], s[16 + i], s[32 + i]);
+                m = max3(m, s[48 + i], s[64 + i]);
+                m = max3(m, s[80 + i], s[96 + i]);
+                a16[i] = fmaxf(m, s[112 + i]);
+            }
+            float mx = max3(max3(a16[0], a16[1], a16[2]), max3(a16[3], a16[4], a16[5]), max3(a16[6], a16[7], a16[8]));
+            mx = max3(mx, max3(a16[9], a16[10], a16[11]), max3(a16[12], a16[13], a16[14]));
+            mx = fmaxf(mx, a16[15]);
             const float m_new = fmaxf(m_used, mx * sl2);
             const bool need = m_new > m_used + 8.f;
             if (j == 0) {
@@ -257,14 +266,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 tmem_wait_st();
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;
-            float rs = 0.f;
+            // p = 2^(s scale log2e - m): the arguments two at a time, four independent row sums
+            const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mref, -mref);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[kTileRows / 2];
 #pragma unroll
             for (int c = 0; c < kTileRows / 2; ++c) {
-                const float a = ex2(fmaf(s[2 * c], sl2, -mref));
-                const float b = ex2(fmaf(s[2 * c + 1], sl2, -mref));
-                rs += a + b;
+                float xa, xb;
+                f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sc2, nm2), xa, xb);
+                const float a = ex2(xa), b = ex2(xb);
+                acc[c & 3] = f2_add(acc[c & 3], f2_pack(a, b));
                 pk[c] = pack_bf16(a, b);
+            }
+            float rs;
+            {
+                float r0, r1, r2, r3, r4, r5, r6, r7;
+                f2_unpack(acc[0], r0, r1);
+                f2_unpack(acc[1], r2, r3);
+                f2_unpack(acc[2], r4, r5);
+                f2_unpack(acc[3], r6, r7);
+                rs = ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
             }
             l += rs;
             tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
