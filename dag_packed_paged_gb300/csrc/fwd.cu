@@ -89,7 +89,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_init(q_full, 1);
         for (int s = 0; s < kKS; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
         for (int s = 0; s < kVS; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
-        for (int t = 0; t < 2; ++t) { mbar_init(s_full(t), 1); mbar_init(p_full(t), 128); }
+        for (int t = 0; t < 2; ++t) { mbar_init(s_full(t), 1); mbar_init(p_full(t), 4); }   // one arrival per warp
         mbar_init(o_full, 1);
         *abort = 0;
         fence_barrier_init();
@@ -292,7 +292,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full(t));
+            __syncwarp();                            // the whole warp's P is in TMEM
+            if (lane == 0) mbar_arrive(p_full(t));
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
