@@ -11,6 +11,7 @@
 
 #include "kernels.h"
 #include "plan.h"
+#include "ptx.cuh"
 
 namespace treeattn {
 
@@ -265,11 +266,16 @@ int tree_attn_check(const ta_plan *plan, void *stream) {
     int32_t st[4] = {0, 0, 0, 0};
     e = cudaMemcpy(st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (st[0] | st[1] | st[2] | st[3]) {
+    const int32_t any = st[0] | st[1] | st[2] | st[3];
+    if (any) {
         cudaMemset(plan->d_status, 0, sizeof(st));
         cudaDeviceSynchronize();
-        set_error("a bounded device-side wait expired; outputs of the affected launches are invalid");
-        return TA_ERR_DEVICE_TIMEOUT;
+        if (any & kStatusTimeout) {
+            set_error("a bounded device-side wait expired; outputs of the affected launches are invalid");
+            return TA_ERR_DEVICE_TIMEOUT;
+        }
+        set_error("a kernel found its dynamic shared memory misaligned and did nothing; outputs are invalid");
+        return TA_ERR_CUDA;
     }
     return TA_OK;
 }

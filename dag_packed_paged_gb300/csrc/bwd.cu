@@ -88,7 +88,8 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t 
 }
 
 constexpr int kBwdThreads = 320;   // warps 0-3 / 4-7: elementwise groups, 8 loads, 9 MMA
-constexpr int kStages = 2;         // dK/dV: Q/dO stages
+constexpr int kQStages = 3;        // dK/dV: Q stages (a Q tile is last read by dK)
+constexpr int kDoStages = 2;       // dK/dV: dO stages (a dO tile is last read by dV)
 constexpr int kKStages = 3;        // dQ: K stages (K is held until the dQ MMAs)
 constexpr int kVStages = 3;        // dQ: V stages (V is released after the dP MMAs)
 
@@ -386,12 +387,17 @@ struct DkvLayout {
     static constexpr int kTile = 128 * D * 2;
     static constexpr int k_off = 0;
     static constexpr int v_off = k_off + kTile;
-    static constexpr int q_off = v_off + kTile;                 // stage s: Q at q_off + s*2*kTile, dO after it
-    static constexpr int lse_off = q_off + kStages * 2 * kTile; // stage s: the unit table (128 lse2 + 128 delta)
-    static constexpr int bar_off = lse_off + kStages * 256 * 4;
-    static constexpr int n_bars = 1 + 2 * kStages + 4 + 1;
+    static constexpr int q_off = v_off + kTile;                    // kQStages Q tiles
+    static constexpr int do_off = q_off + kQStages * kTile;        // kDoStages dO tiles
+    // the unit's lse*log2(e) travels with its dO tile (read by the first elementwise phase, which
+    // ends before dV can release the dO slot), its delta with its Q tile (read by the second
+    // phase, which ends before dK releases the Q slot)
+    static constexpr int lse_off = do_off + kDoStages * kTile;     // per dO stage: 128 floats
+    static constexpr int dl_off = lse_off + kDoStages * 512;       // per Q stage: 128 floats
+    static constexpr int bar_off = dl_off + kQStages * 512;
+    static constexpr int n_bars = 1 + 2 * kQStages + 2 * kDoStages + 5;
     static constexpr int misc_off = bar_off + n_bars * 8;
-    static constexpr int bytes = misc_off + 16 + 1024;
+    static constexpr int bytes = misc_off + 16;                     // the base is 1024-aligned
 };
 
 // One CTA = one key tile x one KV head x one chunk of the tile's readers.  K and V stay in
@@ -405,14 +411,22 @@ struct DkvLayout {
 // The two elementwise warpgroups split each unit's 128 query columns (64 each); P stays in
 // their registers between the phases.  dV and dK accumulate in TMEM for the whole chunk and
 // each key row of the tile is written once at the end.
+// Q and dO have separate rings: a unit's dO is last read by dV (early in its period), its Q
+// by dK (late), so three Q slots and two dO slots give both about two periods between the
+// release of a slot and the first read of the tile loaded into it -- the load latency of a
+// 32 KB tile on these access patterns is about 3,000 cycles.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
     using L = DkvLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {                      // the layout has no alignment slack left
+        if (threadIdx.x == 0) atomicOr(p.status, kStatusMisaligned);
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int ci = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
@@ -422,22 +436,26 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int U = 2 * n_ent;   // (entry, query tile) units
 
     const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off;
-    auto sQ = [&](int s) { return sbase + L::q_off + s * 2 * L::kTile; };
-    auto sDO = [&](int s) { return sbase + L::q_off + s * 2 * L::kTile + L::kTile; };
-    float *lse_s = reinterpret_cast<float *>(smem + L::lse_off);     // [stage][256]
+    auto sQ = [&](int s) { return sbase + L::q_off + s * L::kTile; };
+    auto sDO = [&](int s) { return sbase + L::do_off + s * L::kTile; };
+    float *lse_s = reinterpret_cast<float *>(smem + L::lse_off);      // [dO stage][128]
+    float *dl_s = reinterpret_cast<float *>(smem + L::dl_off);        // [Q stage][128]
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
     const uint32_t kv_full = bar(0);
-    auto qd_full = [&](int s) { return bar(1 + s); };
-    auto qd_empty = [&](int s) { return bar(1 + kStages + s); };
-    const uint32_t s_full = bar(1 + 2 * kStages), dp_full = bar(2 + 2 * kStages);
-    const uint32_t p_full = bar(3 + 2 * kStages), ds_full = bar(4 + 2 * kStages);
-    const uint32_t o_full = bar(5 + 2 * kStages);
+    auto q_full = [&](int s) { return bar(1 + s); };
+    auto q_empty = [&](int s) { return bar(1 + kQStages + s); };
+    auto do_full = [&](int s) { return bar(1 + 2 * kQStages + s); };
+    auto do_empty = [&](int s) { return bar(1 + 2 * kQStages + kDoStages + s); };
+    constexpr int kb = 1 + 2 * kQStages + 2 * kDoStages;
+    const uint32_t s_full = bar(kb), dp_full = bar(kb + 1), p_full = bar(kb + 2), ds_full = bar(kb + 3);
+    const uint32_t o_full = bar(kb + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int s = 0; s < kStages; ++s) { mbar_init(qd_full(s), 1); mbar_init(qd_empty(s), 1); }
+        for (int s = 0; s < kQStages; ++s) { mbar_init(q_full(s), 1); mbar_init(q_empty(s), 1); }
+        for (int s = 0; s < kDoStages; ++s) { mbar_init(do_full(s), 1); mbar_init(do_empty(s), 1); }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
         mbar_init(p_full, 256);
@@ -474,34 +492,45 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tma_kv_tile(sV, &tm_v, ky, ppt, p.page_size, g, D, kv_full);
         }
         int4 mine = make_int4(0, 0, 0, 0);   // lane i holds the reader info of entry (base + i)
-        int issued = 0;
+        int q_issued = 0, do_issued = 0;
         for (int u = 0; u < U; ++u) {
-            const int s = u % kStages, t = u & 1, e = u >> 1;
+            const int qs = u % kQStages, ds = u % kDoStages, t = u & 1, e = u >> 1;
             if ((u & 63) == 0 && e + lane < n_ent) mine = __ldg(tinfo + e + lane);
             const int qb = __shfl_sync(0xffffffffu, mine.x, e & 31) >> 2;
             const int q_row0 = __shfl_sync(0xffffffffu, mine.y, e & 31);
             bool ok = true;
-            if (lane == 0 && u >= kStages) ok = mbar_wait(qd_empty(s), ((u / kStages) - 1) & 1, abort, p.status);
+            // dO first: its slot frees earlier in the period (after dV) than a Q slot (after dK)
+            if (lane == 0 && u >= kDoStages) ok = mbar_wait(do_empty(ds), ((u / kDoStages) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            const float *utab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(do_full(ds), L::kTile + 512);
+                bulk_load(smem_u32(lse_s + ds * 128), utab, 512, do_full(ds));
+                load_q_tile(sDO(ds), &tm_do, t, g, p.G, p.R, D, q_row0, do_full(ds));
+            }
+            do_issued = u + 1;
+            if (lane == 0 && u >= kQStages) ok = mbar_wait(q_empty(qs), ((u / kQStages) - 1) & 1, abort, p.status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(qd_full(s), 2 * L::kTile + 1024);
-                bulk_load(smem_u32(lse_s + s * 256), p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256,
-                          1024, qd_full(s));
-                load_q_tile(sQ(s), &tm_q, t, g, p.G, p.R, D, q_row0, qd_full(s));
-                load_q_tile(sDO(s), &tm_do, t, g, p.G, p.R, D, q_row0, qd_full(s));
+                mbar_arrive_expect_tx(q_full(qs), L::kTile + 512);
+                bulk_load(smem_u32(dl_s + qs * 128), utab + 128, 512, q_full(qs));
+                load_q_tile(sQ(qs), &tm_q, t, g, p.G, p.R, D, q_row0, q_full(qs));
             }
-            issued = u + 1;
+            q_issued = u + 1;
         }
         if (lane == 0) {
-            for (int d = (issued > kStages ? issued - kStages : 0); d < issued; ++d)
-                mbar_wait(qd_full(d % kStages), (d / kStages) & 1, nullptr, p.status);
+            for (int d = (do_issued > kDoStages ? do_issued - kDoStages : 0); d < do_issued; ++d)
+                mbar_wait(do_full(d % kDoStages), (d / kDoStages) & 1, nullptr, p.status);
+            for (int d = (q_issued > kQStages ? q_issued - kQStages : 0); d < q_issued; ++d)
+                mbar_wait(q_full(d % kQStages), (d / kQStages) & 1, nullptr, p.status);
             mbar_wait(kv_full, 0, nullptr, p.status);
         }
     } else if (warp == 9) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(qd_full(0), 0, abort, p.status);
+            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(q_full(0), 0, abort, p.status) &&
+                      mbar_wait(do_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
                 issue_qk<D>(tmem + cS, sK, sQ(0), idesc_s);        // S^T = K Q^T
@@ -510,22 +539,26 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mma_commit(dp_full);
             }
             for (int u = 0; ok && u < U; ++u) {
-                const int s = u % kStages, s1 = (u + 1) % kStages;
+                const int qs = u % kQStages, ds = u % kDoStages;
+                const int qs1 = (u + 1) % kQStages, ds1 = (u + 1) % kDoStages;
                 if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc_split(tmem + cDV, tmem + cS, sDO(s), idesc_o, u > 0);    // dV += P^T dO
+                issue_acc_split(tmem + cDV, tmem + cS, sDO(ds), idesc_o, u > 0);    // dV += P^T dO
+                mma_commit(do_empty(ds));
                 if (u + 1 < U) {
-                    if (!(ok = mbar_wait(qd_full(s1), ((u + 1) / kStages) & 1, abort, p.status))) break;
+                    if (!(ok = mbar_wait(q_full(qs1), ((u + 1) / kQStages) & 1, abort, p.status))) break;
                     tc_fence_after();
-                    issue_qk<D>(tmem + cS, sK, sQ(s1), idesc_s);
+                    issue_qk<D>(tmem + cS, sK, sQ(qs1), idesc_s);
                     mma_commit(s_full);
                 }
                 if (!(ok = mbar_wait(ds_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc_split(tmem + cDK, tmem + cDP, sQ(s), idesc_o, u > 0);    // dK += dS^T Q
-                mma_commit(qd_empty(s));
+                issue_acc_split(tmem + cDK, tmem + cDP, sQ(qs), idesc_o, u > 0);    // dK += dS^T Q
+                mma_commit(q_empty(qs));
                 if (u + 1 < U) {
-                    issue_qk<D>(tmem + cDP, sV, sDO(s1), idesc_s);
+                    if (!(ok = mbar_wait(do_full(ds1), ((u + 1) / kDoStages) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    issue_qk<D>(tmem + cDP, sV, sDO(ds1), idesc_s);
                     mma_commit(dp_full);
                 }
             }
@@ -542,16 +575,16 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         bool ok = true;
         WarpRecords recs;
         for (int u = 0; u < U; ++u) {
-            const int s = u % kStages;
+            const int ds = u % kDoStages, qs = u % kQStages;
             const int4 te = recs.get(tinfo, u >> 1, n_ent, lane);
-            // s_full implies the stage was loaded; waiting on qd_full as well makes the bulk-copied
-            // table visible to this thread directly
+            // s_full implies the unit's stages were loaded; waiting on their barriers as well makes
+            // the bulk-copied lse / delta visible to this thread directly
             ok = __all_sync(0xffffffffu, mbar_wait(s_full, u & 1, abort, p.status) &&
-                                             mbar_wait(qd_full(s), (u / kStages) & 1, abort, p.status));
+                                             mbar_wait(do_full(ds), (u / kDoStages) & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
-            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + s * 256 + 64 * w);
-            const float4 *dl4 = reinterpret_cast<const float4 *>(lse_s + s * 256 + 128 + 64 * w);
+            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + ds * 128 + 64 * w);
+            const float4 *dl4 = reinterpret_cast<const float4 *>(dl_s + qs * 128 + 64 * w);
             const bool row_in = jj >= te.z && jj < te.w;
             const bool causal = (te.x & kEntryCausal) != 0;
             // query row of lane m of this group's columns: first row + ((128 t + 64 w + m) mod R)
@@ -593,7 +626,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 mbar_arrive(p_full);
             }
             // ---------------- phase 2: dS^T
-            ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, abort, p.status));
+            ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, abort, p.status) &&
+                                             mbar_wait(q_full(qs), (u / kQStages) & 1, abort, p.status));
             if (!ok) break;
             tc_fence_after();
             {

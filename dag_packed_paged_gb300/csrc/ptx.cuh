@@ -13,6 +13,7 @@ constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait, then gi
 
 // status bits (device word, read by tree_attn_check)
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusMisaligned = 2;   // dynamic shared memory not 1024-byte aligned: kernel did nothing
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
