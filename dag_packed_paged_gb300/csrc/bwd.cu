@@ -7,8 +7,8 @@
 // "differentiable mount edges", HARTS arXiv 2608.28158 Section 3.4 gather backward).
 //
 // Four launches:
-//   delta_kernel   per (query block, KV head, 128-lane query tile): each lane's lse * log2(e)
-//                  and delta = <dO, O>, one 1 KB table per tile                (HBM-bound)
+//   delta_kernel   per (query block, KV head, 128-lane query tile): each lane's -lse * log2(e)
+//                  and -delta = -<dO, O>, one 1 KB table per tile              (HBM-bound)
 //   dq_kernel      query-major: one CTA per (query block, KV head, 128-lane query tile);
 //                  walks the block's key-tile entries like the forward
 //   dkdv_kernel    key-major: one CTA per (key-tile chunk, KV head); walks the query blocks
@@ -29,9 +29,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ------------------------------------------------------------------------------ delta
 // One CTA per (query block, KV head, 128-lane query tile); thread m handles query lane m,
 // i.e. row (head hl, row rl) with 128 t + m = hl R + rl.  It writes the tile's 1 KB unit
-// table: [m] = lse * log2(e) (+inf for padding lanes, so that P = 0 there) and
-// [128 + m] = delta = <dO, O> of that row.  Both backward kernels read these per-lane
-// values from the table; the dK/dV loader copies a whole tile's table with one bulk copy.
+// table: [m] = -lse * log2(e) (-inf for padding lanes, so that P = 0 there) and
+// [128 + m] = -delta = -<dO, O> of that row, negated so that both backward kernels add
+// them (P = exp2(S scale log2e + [m]), dS = P (dP + [128 + m])).  The dK/dV loader copies
+// the halves with one bulk copy each.
 template <int D>
 __global__ void __launch_bounds__(128) delta_kernel(const BwdParams p) {
     const int t = blockIdx.x & 1, g = (blockIdx.x >> 1) % p.Hkv, qb = (blockIdx.x >> 1) / p.Hkv;
@@ -39,7 +40,7 @@ __global__ void __launch_bounds__(128) delta_kernel(const BwdParams p) {
     const int hl = m_flat / p.R, rl = m_flat % p.R, h = g * p.G + hl;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
     const bool valid = rl < n_rows;
-    float lse2 = INFINITY, acc = 0.f;
+    float nlse2 = -INFINITY, acc = 0.f;
     if (valid) {
         const int r = q_row0 + rl;
         const size_t base = (static_cast<size_t>(r) * p.Hq + h) * D;
@@ -57,11 +58,11 @@ __global__ void __launch_bounds__(128) delta_kernel(const BwdParams p) {
                 acc = fmaf(fx.y, fy.y, acc);
             }
         }
-        lse2 = __ldg(p.lse + static_cast<size_t>(h) * p.N + r) * kLog2e;
+        nlse2 = -__ldg(p.lse + static_cast<size_t>(h) * p.N + r) * kLog2e;
     }
     float *tab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
-    tab[m] = lse2;
-    tab[128 + m] = acc;
+    tab[m] = nlse2;
+    tab[128 + m] = -acc;
 }
 
 // One 128-lane query tile t of a block: rows (head, row) flattened as m = hl * R + rl.
@@ -304,8 +305,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         mbar_arrive(qd_ready);
         const float sl2 = p.scale_log2;
         const float *tab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
-        const float lse2 = tab[32 * q4 + lane];
-        const float delta = tab[128 + 32 * q4 + lane];
+        const float nlse2 = tab[32 * q4 + lane];      // -lse * log2(e)
+        const float ndelta = tab[128 + 32 * q4 + lane];  // -delta
         bool ok = true;
         WarpRecords recs;
         for (int j = 0; j < E; ++j) {
@@ -323,7 +324,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tc_fence_before();
                 mbar_arrive(s_free);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) pf[i] = ex2(fmaf(__uint_as_float(sv[i >> 5][i & 31]), sl2, -lse2));
+                for (int i = 0; i < 64; ++i) pf[i] = ex2(fmaf(__uint_as_float(sv[i >> 5][i & 31]), sl2, nlse2));
                 if (e.w != 0) {                      // partial / diagonal tile: mask key columns
                     const int j0 = e.x * kTileRows + 64 * w;
                     const int lo = e.y - j0;
@@ -344,8 +345,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 uint32_t ds[2][16];
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    ds[i >> 4][i & 15] = pack_bf16(pf[2 * i] * (__uint_as_float(dpv[i >> 4][(2 * i) & 31]) - delta),
-                                                   pf[2 * i + 1] * (__uint_as_float(dpv[i >> 4][(2 * i + 1) & 31]) - delta));
+                    ds[i >> 4][i & 15] = pack_bf16(pf[2 * i] * (__uint_as_float(dpv[i >> 4][(2 * i) & 31]) + ndelta),
+                                                   pf[2 * i + 1] * (__uint_as_float(dpv[i >> 4][(2 * i + 1) & 31]) + ndelta));
                 tmem_st16(tmem + lane_off + cDP + 64 * w, ds[0]);
                 tmem_st16(tmem + lane_off + cDP + 64 * w + 16, ds[1]);
                 tmem_wait_st();
@@ -499,24 +500,25 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const int qb = __shfl_sync(0xffffffffu, mine.x, e & 31) >> 2;
             const int q_row0 = __shfl_sync(0xffffffffu, mine.y, e & 31);
             bool ok = true;
-            // dO first: its slot frees earlier in the period (after dV) than a Q slot (after dK)
-            if (lane == 0 && u >= kDoStages) ok = mbar_wait(do_empty(ds), ((u / kDoStages) - 1) & 1, abort, p.status);
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-            const float *utab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(do_full(ds), L::kTile + 512);
-                bulk_load(smem_u32(lse_s + ds * 128), utab, 512, do_full(ds));
-                load_q_tile(sDO(ds), &tm_do, t, g, p.G, p.R, D, q_row0, do_full(ds));
-            }
-            do_issued = u + 1;
+            // Q first: S^T(u) is the first MMA to read the unit, dP^T(u) comes after it; the slots
+            // free in the same order (dK(u-3) completes before dV(u-2))
             if (lane == 0 && u >= kQStages) ok = mbar_wait(q_empty(qs), ((u / kQStages) - 1) & 1, abort, p.status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            const float *utab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
             if (lane == 0) {
                 mbar_arrive_expect_tx(q_full(qs), L::kTile + 512);
                 bulk_load(smem_u32(dl_s + qs * 128), utab + 128, 512, q_full(qs));
                 load_q_tile(sQ(qs), &tm_q, t, g, p.G, p.R, D, q_row0, q_full(qs));
             }
             q_issued = u + 1;
+            if (lane == 0 && u >= kDoStages) ok = mbar_wait(do_empty(ds), ((u / kDoStages) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(do_full(ds), L::kTile + 512);
+                bulk_load(smem_u32(lse_s + ds * 128), utab, 512, do_full(ds));
+                load_q_tile(sDO(ds), &tm_do, t, g, p.G, p.R, D, q_row0, do_full(ds));
+            }
+            do_issued = u + 1;
         }
         if (lane == 0) {
             for (int d = (do_issued > kDoStages ? do_issued - kDoStages : 0); d < do_issued; ++d)
@@ -596,24 +598,27 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tmem_ld32(tmem + lane_off + cS + 64 * w, sv[0]);
                 tmem_ld32(tmem + lane_off + cS + 64 * w + 32, sv[1]);
                 tmem_wait_ld();
-                if (!row_in) {
+                // all 64 columns branch-free, two at a time; masks (rows outside the entry, the
+                // causal triangle) in a separate pass only where some lane needs them
+                const uint64_t sc2 = f2_pack(sl2, sl2);
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) pf[i] = 0.f;
-                } else {
+                for (int i4 = 0; i4 < 16; ++i4) {
+                    const float4 l4 = ls4[i4];       // -lse * log2(e) of four query columns
+                    float x0, x1, x2, x3;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i4 >> 3][4 * (i4 & 7)]), __uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + 1])),
+                                     sc2, f2_pack(l4.x, l4.y)), x0, x1);
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + 2]), __uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + 3])),
+                                     sc2, f2_pack(l4.z, l4.w)), x2, x3);
+                    pf[4 * i4] = ex2(x0);
+                    pf[4 * i4 + 1] = ex2(x1);
+                    pf[4 * i4 + 2] = ex2(x2);
+                    pf[4 * i4 + 3] = ex2(x3);
+                }
+                if (causal || __any_sync(0xffffffffu, !row_in)) {
 #pragma unroll
-                    for (int i4 = 0; i4 < 16; ++i4) {
-                        const float4 l4 = ls4[i4];
-                        const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            pf[4 * i4 + v] = ex2(fmaf(__uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + v]), sl2, -lq[v]));
-                        if (causal) {
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const int r = rbase + ((mbase + 4 * i4 + v) & rmask);
-                                pf[4 * i4 + v] = jj > r ? 0.f : pf[4 * i4 + v];
-                            }
-                        }
+                    for (int c = 0; c < 64; ++c) {
+                        const int r = rbase + ((mbase + c) & rmask);
+                        pf[c] = (row_in && !(causal && jj > r)) ? pf[c] : 0.f;
                     }
                 }
                 uint32_t pk[2][16];
@@ -638,14 +643,16 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 uint32_t dk[2][16];
 #pragma unroll
                 for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 d4 = dl4[i4];
-                    const float dq4[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float dr[4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dr[v] = pf[4 * i4 + v] * (__uint_as_float(dv[i4 >> 3][4 * (i4 & 7) + v]) - dq4[v]);
-                    dk[i4 >> 3][2 * (i4 & 7)] = pack_bf16(dr[0], dr[1]);
-                    dk[i4 >> 3][2 * (i4 & 7) + 1] = pack_bf16(dr[2], dr[3]);
+                    const float4 d4 = dl4[i4];       // -delta of four query columns
+                    float r0, r1, r2, r3;
+                    f2_unpack(f2_mul(f2_pack(pf[4 * i4], pf[4 * i4 + 1]),
+                                     f2_add(f2_pack(__uint_as_float(dv[i4 >> 3][4 * (i4 & 7)]), __uint_as_float(dv[i4 >> 3][4 * (i4 & 7) + 1])),
+                                            f2_pack(d4.x, d4.y))), r0, r1);
+                    f2_unpack(f2_mul(f2_pack(pf[4 * i4 + 2], pf[4 * i4 + 3]),
+                                     f2_add(f2_pack(__uint_as_float(dv[i4 >> 3][4 * (i4 & 7) + 2]), __uint_as_float(dv[i4 >> 3][4 * (i4 & 7) + 3])),
+                                            f2_pack(d4.z, d4.w))), r2, r3);
+                    dk[i4 >> 3][2 * (i4 & 7)] = pack_bf16(r0, r1);
+                    dk[i4 >> 3][2 * (i4 & 7) + 1] = pack_bf16(r2, r3);
                 }
                 tmem_st16(tmem + lane_off + cDP + 64 * w, dk[0]);
                 tmem_st16(tmem + lane_off + cDP + 64 * w + 16, dk[1]);

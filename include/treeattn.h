@@ -234,7 +234,7 @@ int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const void *k_pool
                           float *dv_pool, void *stream);
 
 /* Bytes of device scratch tree_attn_bwd needs for this plan: a 1 KB table per (KV head, query
- * block, 128-lane query tile) holding lse * log2(e) and delta, plus dK/dV partial slots. */
+ * block, 128-lane query tile) holding -lse * log2(e) and -delta, plus dK/dV partial slots. */
 size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
 
 /* Synchronises `stream` and reports whether any bounded device wait of this plan's kernels
