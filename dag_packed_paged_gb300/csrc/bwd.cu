@@ -323,8 +323,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(s_free);
+                const uint64_t sc2 = f2_pack(sl2, sl2), nl2 = f2_pack(nlse2, nlse2);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) pf[i] = ex2(fmaf(__uint_as_float(sv[i >> 5][i & 31]), sl2, nlse2));
+                for (int i = 0; i < 32; ++i) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]), __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
+                                     sc2, nl2), x0, x1);
+                    pf[2 * i] = ex2(x0);
+                    pf[2 * i + 1] = ex2(x1);
+                }
                 if (e.w != 0) {                      // partial / diagonal tile: mask key columns
                     const int j0 = e.x * kTileRows + 64 * w;
                     const int lo = e.y - j0;
@@ -343,10 +350,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_ld32(tmem + lane_off + cDP + 64 * w + 32, dpv[1]);
                 tmem_wait_ld();
                 uint32_t ds[2][16];
+                const uint64_t nd2 = f2_pack(ndelta, ndelta);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    ds[i >> 4][i & 15] = pack_bf16(pf[2 * i] * (__uint_as_float(dpv[i >> 4][(2 * i) & 31]) + ndelta),
-                                                   pf[2 * i + 1] * (__uint_as_float(dpv[i >> 4][(2 * i + 1) & 31]) + ndelta));
+                for (int i = 0; i < 32; ++i) {
+                    float r0, r1;
+                    f2_unpack(f2_mul(f2_pack(pf[2 * i], pf[2 * i + 1]),
+                                     f2_add(f2_pack(__uint_as_float(dpv[i >> 4][(2 * i) & 31]), __uint_as_float(dpv[i >> 4][(2 * i + 1) & 31])),
+                                            nd2)), r0, r1);
+                    ds[i >> 4][i & 15] = pack_bf16(r0, r1);
+                }
                 tmem_st16(tmem + lane_off + cDP + 64 * w, ds[0]);
                 tmem_st16(tmem + lane_off + cDP + 64 * w + 16, ds[1]);
                 tmem_wait_st();
