@@ -89,6 +89,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t 
 }
 
 constexpr int kBwdThreads = 320;   // warps 0-3 / 4-7: elementwise groups, 8 loads, 9 MMA
+constexpr int kDkvThreads = 352;   // dK/dV: warps 9 and 10 each issue one of the two MMA chains
 constexpr int kQStages = 3;        // dK/dV: Q stages (a Q tile is last read by dK)
 constexpr int kDoStages = 2;       // dK/dV: dO stages (a dO tile is last read by dV)
 constexpr int kKStages = 3;        // dQ: K stages (K is held until the dQ MMAs)
@@ -428,8 +429,13 @@ struct DkvLayout {
 // by dK (late), so three Q slots and two dO slots give both about two periods between the
 // release of a slot and the first read of the tile loaded into it -- the load latency of a
 // 32 KB tile on these access patterns is about 3,000 cycles.
+// The two MMA chains have their own issuing threads -- warp 9: S^T(u+1) after dV(u) (both on
+// the S^T columns), warp 10: dP^T(u+1) after dK(u) (the dP^T columns) -- because issuing a
+// batch of MMAs blocks the thread until the tensor core has room, and one thread would only
+// see the other chain's barrier after its own batch.  A Q or dO slot is read by MMAs of both
+// chains, so its "empty" barrier takes one commit from each.
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkvThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
     using L = DkvLayout<D>;
@@ -467,13 +473,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int s = 0; s < kQStages; ++s) { mbar_init(q_full(s), 1); mbar_init(q_empty(s), 1); }
-        for (int s = 0; s < kDoStages; ++s) { mbar_init(do_full(s), 1); mbar_init(do_empty(s), 1); }
+        for (int s = 0; s < kQStages; ++s) { mbar_init(q_full(s), 1); mbar_init(q_empty(s), 2); }
+        for (int s = 0; s < kDoStages; ++s) { mbar_init(do_full(s), 1); mbar_init(do_empty(s), 2); }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
         mbar_init(p_full, 256);
         mbar_init(ds_full, 256);
-        mbar_init(o_full, 1);
+        mbar_init(o_full, 2);
         *abort = 0;
         fence_barrier_init();
     }
@@ -540,21 +546,19 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             mbar_wait(kv_full, 0, nullptr, p.status);
         }
     } else if (warp == 9) {
+        // ---------------------------------------------------------------- MMA: S^T, dV chain
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(q_full(0), 0, abort, p.status) &&
-                      mbar_wait(do_full(0), 0, abort, p.status);
+            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(q_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
                 issue_qk<D>(tmem + cS, sK, sQ(0), idesc_s);        // S^T = K Q^T
                 mma_commit(s_full);
-                issue_qk<D>(tmem + cDP, sV, sDO(0), idesc_s);      // dP^T = V dO^T
-                mma_commit(dp_full);
+                mma_commit(q_empty(0));                            // this chain's read of Q(0)
             }
             for (int u = 0; ok && u < U; ++u) {
-                const int qs = u % kQStages, ds = u % kDoStages;
-                const int qs1 = (u + 1) % kQStages, ds1 = (u + 1) % kDoStages;
+                const int ds = u % kDoStages, qs1 = (u + 1) % kQStages;
                 if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
                 issue_acc_split(tmem + cDV, tmem + cS, sDO(ds), idesc_o, u > 0);    // dV += P^T dO
@@ -564,7 +568,26 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc_fence_after();
                     issue_qk<D>(tmem + cS, sK, sQ(qs1), idesc_s);
                     mma_commit(s_full);
+                    mma_commit(q_empty(qs1));
                 }
+            }
+            mma_commit(o_full);
+            mbar_wait(o_full, 0, nullptr, p.status);
+        }
+    } else if (warp == 10) {
+        // ---------------------------------------------------------------- MMA: dP^T, dK chain
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
+            bool ok = U > 0 && mbar_wait(kv_full, 0, abort, p.status) && mbar_wait(do_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_qk<D>(tmem + cDP, sV, sDO(0), idesc_s);      // dP^T = V dO^T
+                mma_commit(dp_full);
+                mma_commit(do_empty(0));                           // this chain's read of dO(0)
+            }
+            for (int u = 0; ok && u < U; ++u) {
+                const int qs = u % kQStages, ds1 = (u + 1) % kDoStages;
                 if (!(ok = mbar_wait(ds_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
                 issue_acc_split(tmem + cDK, tmem + cDP, sQ(qs), idesc_o, u > 0);    // dK += dS^T Q
@@ -574,6 +597,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc_fence_after();
                     issue_qk<D>(tmem + cDP, sV, sDO(ds1), idesc_s);
                     mma_commit(dp_full);
+                    mma_commit(do_empty(ds1));
                 }
             }
             mma_commit(o_full);
@@ -754,7 +778,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
     e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::bytes);
     if (e != cudaSuccess) return e;
     trace_record(trace, 4, stream);
-    dkdv_kernel<D><<<n_chunks * p.Hkv, kBwdThreads, DkvLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    dkdv_kernel<D><<<n_chunks * p.Hkv, kDkvThreads, DkvLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     trace_record(trace, 5, stream);
     if (n_reduce > 0) {
