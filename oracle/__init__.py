@@ -72,12 +72,15 @@ class Result:
         self.threads = 0
 
 
-def forward(branches, mounts, q, k, v, scale, rows=None, intervals=None, n_threads=0) -> Result:
-    """O and lse (natural log) of the listed rows (default: all rows)."""
+def forward(branches, mounts, q, k, v, scale, rows=None, intervals=None, n_threads=0,
+            view="mounted") -> Result:
+    """O and lse (natural log) of the listed rows (default: all rows); ``view`` selects the
+    visibility (see ``dag.VIEWS``)."""
     N, Hq, D = q.shape
     Hkv = k.shape[1]
     if intervals is None:
-        intervals = dag.visible_intervals(branches, mounts, rows)
+        intervals = dag.visible_intervals(branches, mounts, rows) if view == "mounted" else \
+            dag.visible_intervals(branches, mounts, rows, view=view)
     rws, ptr, lo, hi = (_c(x, np.int64) for x in intervals)
     n = len(rws)
     res = Result(rws)
@@ -115,8 +118,9 @@ def backward(branches, mounts, q, k, v, do, scale, fwd: Result, with_dkdv=True,
     return res
 
 
-def run(branches, mounts, q, k, v, do, scale, rows=None, with_dkdv=True, n_threads=0) -> Result:
+def run(branches, mounts, q, k, v, do, scale, rows=None, with_dkdv=True, n_threads=0,
+        view="mounted") -> Result:
     """Forward then backward for the listed rows (default: all rows)."""
-    f = forward(branches, mounts, q, k, v, scale, rows=rows, n_threads=n_threads)
+    f = forward(branches, mounts, q, k, v, scale, rows=rows, n_threads=n_threads, view=view)
     return backward(branches, mounts, q, k, v, do, scale, f, with_dkdv=with_dkdv,
                     n_threads=n_threads)

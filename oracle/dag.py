@@ -25,6 +25,15 @@ Readings where the pages are silent (each listed in the design notes):
 * a child forking at offset f inherits its parent's rows [0, f), the parent's mounts active
   at row f-1, and everything the parent inherited (for f = 0 only the latter);
 * a zero-length mount contributes no rows and no position jump.
+
+Two further views of the same episode (same rows, same Eq. 2 positions):
+* ``view="no_mounts"`` -- layers that do not mount (Octopus Section 3.2, layer-selective
+  mounting; Appendix C Table 8, the mounted / unmounted dual pass) see the ancestor path and
+  their own rows only;
+* ``view="transitive"`` -- a node's active mounted segments "including transitive mounts"
+  (Octopus Section 3.3 item 1): a mounted span [s, e) of source A also brings the mounts in
+  effect at A's row e-1 (A's own with reader offset <= e-1 and those A inherits), and so on
+  recursively.
 """
 from __future__ import annotations
 
@@ -54,7 +63,48 @@ def row_owner(branches):
     return out
 
 
-def inherited_pieces(branches, mounts, b):
+VIEWS = ("mounted", "no_mounts", "transitive")
+
+
+def mounts_in_effect(branches, mounts, b, i):
+    """Non-empty mounted spans (source, lo_off, hi_off) in effect at row (b, i): b's own
+    mounts with reader offset <= i, and the mounts b inherits (those of an ancestor p that are
+    active at the fork row f-1 of the edge into p's subtree)."""
+    B, M = _br(branches), _mt(mounts)
+    out = [(s, lo, hi) for (r, t, s, lo, hi) in M if r == b and t <= i and hi > lo]
+    x = b
+    while B[x][0] >= 0:
+        p, f = B[x][0], B[x][1]
+        if f > 0:
+            out += [(s, lo, hi) for (r, t, s, lo, hi) in M if r == p and t <= f - 1 and hi > lo]
+        x = p
+    return out
+
+
+def _closure(branches, mounts, spans):
+    """The spans plus, recursively, the spans in effect at each span's last source row."""
+    out, seen, stack = [], set(), list(spans)
+    while stack:
+        sp = stack.pop()
+        if sp in seen:
+            continue
+        seen.add(sp)
+        out.append(sp)
+        s, lo, hi = sp
+        stack.extend(mounts_in_effect(branches, mounts, s, hi - 1))
+    return out
+
+
+def _spans(branches, mounts, spans, view):
+    if view == "no_mounts":
+        return []
+    if view == "transitive":
+        return _closure(branches, mounts, spans)
+    assert view == "mounted", view
+    return list(spans)
+
+
+def inherited_pieces(branches, mounts, b, view="mounted"):
     """Rows a branch shares with its ancestors, as (branch, lo_off, hi_off) pieces.
 
     inh(root) = {};  inh(b) = rows [0, f) of the parent p  +  rows of p's mounts that are
@@ -65,31 +115,30 @@ def inherited_pieces(branches, mounts, b):
         p, f = B[b][0], B[b][1]
         if f > 0:
             out.append((p, 0, f))
-            for (r, t, s, lo, hi) in M:
-                if r == p and t <= f - 1 and hi > lo:
-                    out.append((s, lo, hi))
+            out += _spans(branches, mounts, [(s, lo, hi) for (r, t, s, lo, hi) in M
+                                             if r == p and t <= f - 1 and hi > lo], view)
         b = p
     return out
 
 
-def visible_pieces(branches, mounts, b, i):
+def visible_pieces(branches, mounts, b, i, view="mounted"):
     """Visible rows of the row at offset i of branch b, as (branch, lo_off, hi_off) pieces:
     own rows 0..i, every non-empty mount of b with reader offset <= i, and inh(b)."""
     M = _mt(mounts)
     out = [(b, 0, i + 1)]
-    for (r, t, s, lo, hi) in M:
-        if r == b and t <= i and hi > lo:
-            out.append((s, lo, hi))
-    out += inherited_pieces(branches, mounts, b)
+    out += _spans(branches, mounts, [(s, lo, hi) for (r, t, s, lo, hi) in M
+                                     if r == b and t <= i and hi > lo], view)
+    out += inherited_pieces(branches, mounts, b) if view == "mounted" else \
+        inherited_pieces(branches, mounts, b, view=view)
     return out
 
 
-def visible_set(branches, mounts, row) -> set:
+def visible_set(branches, mounts, row, view="mounted") -> set:
     """The visible compact rows of ``row`` as an explicit Python set (small cases)."""
     B = _br(branches)
     b, i = row_owner(branches)[row]
     out = set()
-    for (x, lo, hi) in visible_pieces(branches, mounts, b, i):
+    for (x, lo, hi) in visible_pieces(branches, mounts, b, i, view=view):
         rs = B[x][3]
         out.update(range(rs + lo, rs + hi))
     return out
@@ -108,7 +157,7 @@ def visible_intervals_of(branches, mounts, b, i):
     return [(lo, hi) for lo, hi in merged]
 
 
-def visible_intervals(branches, mounts, rows=None):
+def visible_intervals(branches, mounts, rows=None, view="mounted"):
     """CSR of visible intervals for the given compact rows (default: all rows, in order).
 
     Returns (rows int64[n], ptr int64[n+1], lo int64[nnz], hi int64[nnz])."""
@@ -135,7 +184,9 @@ def visible_intervals(branches, mounts, rows=None):
         # everything except the own-row piece depends only on (b, number of mount offsets <= i)
         key = (b, sum(1 for t in offsets_of.get(b, ()) if t <= i))
         if key not in cache:
-            cache[key] = [p for p in visible_pieces(branches, mounts, b, i)[1:]]
+            vp = visible_pieces(branches, mounts, b, i) if view == "mounted" else \
+                visible_pieces(branches, mounts, b, i, view=view)
+            cache[key] = vp[1:]
         pieces = [(b, 0, i + 1)] + cache[key]
         iv = sorted((B[x][3] + lo, B[x][3] + hi) for (x, lo, hi) in pieces)
         merged = []
@@ -152,9 +203,9 @@ def visible_intervals(branches, mounts, rows=None):
             np.array(hi_all, dtype=np.int64))
 
 
-def count_pairs(branches, mounts) -> int:
+def count_pairs(branches, mounts, view="mounted") -> int:
     """Sum over rows of the size of the visible set."""
-    _, ptr, lo, hi = visible_intervals(branches, mounts)
+    _, ptr, lo, hi = visible_intervals(branches, mounts, view=view)
     return int((hi - lo).sum())
 
 
