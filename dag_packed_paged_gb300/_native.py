@@ -20,6 +20,8 @@ TA_ERR_NOMEM = -3
 TA_ERR_CUDA = -4
 TA_ERR_DEVICE_TIMEOUT = -5
 TA_CLAMP_MOUNTS = 0x1
+TA_NO_MOUNTS = 0x2
+TA_TRANSITIVE_MOUNTS = 0x4
 TA_PLAN_HOST_ONLY = 0x100
 
 HEADER = os.path.join(INCLUDE, "treeattn.h")

@@ -123,6 +123,9 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
     P.N = N;
 
     // ------------------------------------------------------------------ mounts
+    const bool no_mounts = (c.flags & TA_NO_MOUNTS) != 0;
+    const bool transitive = (c.flags & TA_TRANSITIVE_MOUNTS) != 0;
+    if (no_mounts && transitive) return fail(TA_ERR_INVALID, "TA_NO_MOUNTS and TA_TRANSITIVE_MOUNTS exclude each other");
     std::vector<Mount> mt;
     for (int i = 0; i < n_mounts; ++i) {
         Mount m{mounts[i].reader, mounts[i].reader_offset, mounts[i].source, mounts[i].src_begin, mounts[i].src_end};
@@ -251,6 +254,46 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
         if (!ok) return fail(TA_ERR_INVALID, "cyclic position dependency (non-causal mount)");
     }
 
+    // ------------------------------------------------------------------ visible mounted spans
+    // Per mount, the compact-row intervals it makes visible: its own span; with
+    // TA_TRANSITIVE_MOUNTS also, recursively, the spans of the mounts in effect at the source's
+    // last mounted row (the source's own mounts up to that row and those it inherits through
+    // its fork points).  With TA_NO_MOUNTS nothing (positions above keep the mounts).
+    std::vector<std::vector<Interval>> span_of(mt.size());
+    {
+        // mounts in effect at row (x, r): x's own with t <= r, then inherited along the parents
+        auto in_effect = [&](int x, int32_t r, std::vector<int> &out) {
+            for (int k : mounts_of[x])
+                if (mt[k].t <= r) out.push_back(k);
+            for (int y = x; par[y] >= 0; y = par[y])
+                if (fork[y] > 0)
+                    for (int k : mounts_of[par[y]])
+                        if (mt[k].t <= fork[y] - 1) out.push_back(k);
+        };
+        std::vector<char> state(mt.size(), 0);   // 0 new, 1 on the stack, 2 done
+        std::function<bool(int)> close = [&](int k) -> bool {
+            if (state[k] == 2) return true;
+            if (state[k] == 1) return false;     // a cycle: impossible for causal mounts
+            state[k] = 1;
+            std::vector<Interval> &v = span_of[k];
+            v.push_back({rs[mt[k].source] + mt[k].lo, rs[mt[k].source] + mt[k].hi});
+            if (transitive) {
+                std::vector<int> eff;
+                in_effect(mt[k].source, mt[k].hi - 1, eff);
+                for (int k2 : eff) {
+                    if (!close(k2)) return false;
+                    v.insert(v.end(), span_of[k2].begin(), span_of[k2].end());
+                }
+                merge_intervals(v);
+            }
+            state[k] = 2;
+            return true;
+        };
+        if (!no_mounts)
+            for (int k = 0; k < (int)mt.size(); ++k)
+                if (!close(k)) return fail(TA_ERR_INVALID, "cyclic transitive mounts");
+    }
+
     // ------------------------------------------------------------------ segments and blocks
     const int R = P.block_rows;
     const int T = kTileRows;
@@ -266,20 +309,23 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
             int p = par[x], f = fork[x];
             if (f > 0) {
                 inh.push_back({rs[p], rs[p] + f});
-                for (int k : mounts_of[p])
-                    if (mt[k].t <= f - 1) inh.push_back({rs[mt[k].source] + mt[k].lo, rs[mt[k].source] + mt[k].hi});
+                if (!no_mounts)
+                    for (int k : mounts_of[p])
+                        if (mt[k].t <= f - 1) inh.insert(inh.end(), span_of[k].begin(), span_of[k].end());
             }
         }
         std::vector<int32_t> cuts{0, len[b]};
-        for (int k : mounts_of[b]) cuts.push_back(mt[k].t);
+        if (!no_mounts)
+            for (int k : mounts_of[b]) cuts.push_back(mt[k].t);
         std::sort(cuts.begin(), cuts.end());
         cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
         for (size_t s = 0; s + 1 < cuts.size(); ++s) {
             const int32_t slo = cuts[s], shi = cuts[s + 1];
             ++P.n_segments;
             std::vector<Interval> base = inh;
-            for (int k : mounts_of[b])
-                if (mt[k].t <= slo) base.push_back({rs[mt[k].source] + mt[k].lo, rs[mt[k].source] + mt[k].hi});
+            if (!no_mounts)
+                for (int k : mounts_of[b])
+                    if (mt[k].t <= slo) base.insert(base.end(), span_of[k].begin(), span_of[k].end());
             for (int32_t qs = slo; qs < shi; qs += R) {
                 const int32_t qe = std::min<int32_t>(qs + R, shi);
                 std::vector<Interval> iv = base;

@@ -43,6 +43,18 @@ extern "C" {
 /* Flags (ta_config.flags). */
 #define TA_CLAMP_MOUNTS 0x1u  /* clamp a mount span to the source's rows instead of rejecting it
                                  (Octopus Appendix A clamps spans to the valid range) */
+#define TA_NO_MOUNTS 0x2u     /* the mount-free view of the same episode, for layers that do
+                                 not mount (Octopus Section 3.2, layer-selective mounting, and
+                                 Appendix C Table 8, the mounted / unmounted dual pass): rows see
+                                 their ancestor path and own earlier rows only.  Mounts are still
+                                 validated and still set the Eq. 2 positions, so pos_ids and the
+                                 row layout equal those of the mounted plan. */
+#define TA_TRANSITIVE_MOUNTS 0x4u /* active mounts "including transitive mounts" (Octopus
+                                 Section 3.3 item 1): a mounted span [s, e) of source A also
+                                 brings, recursively, the mounts in effect at A's row e-1 (A's
+                                 own mounts with reader offset <= e-1 and those A inherits through
+                                 its fork points).  Positions are unchanged.  Excludes
+                                 TA_NO_MOUNTS (TA_ERR_INVALID if both are set). */
 #define TA_PLAN_HOST_ONLY 0x100u /* build the plan on the host only (no device upload, no GPU
                                     needed): for inspection with tree_attn_plan_export/_stats;
                                     tree_attn_fwd/_bwd reject such a plan */

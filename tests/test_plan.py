@@ -35,8 +35,8 @@ def _intervals_to_set_runs(lo, hi):
     return [(int(a), int(b)) for a, b in zip(lo, hi)]
 
 
-def check_plan_against_oracle(ep, rows_to_check=None):
-    plan = host_plan(ep)
+def check_plan_against_oracle(ep, rows_to_check=None, flags=0, view="mounted"):
+    plan = host_plan(ep, flags=flags)
     ex = ta.tree_attn_plan_export(plan)
     st = ta.tree_attn_plan_stats(plan)
     N = ep.n_rows
@@ -44,7 +44,7 @@ def check_plan_against_oracle(ep, rows_to_check=None):
     assert (ex["pos_ids"] == dag.positions(ep.branches, ep.mounts)).all()
     assert (plan.pos_ids == ex["pos_ids"]).all()
     # visible sets: per row, block intervals + own rows [diag_lo, r] == oracle enumeration
-    rows, ptr, olo, ohi = dag.visible_intervals(ep.branches, ep.mounts)
+    rows, ptr, olo, ohi = dag.visible_intervals(ep.branches, ep.mounts, view=view)
     blocks, diag, ivp = ex["blocks"], ex["diag"], ex["blk_iv_ptr"]
     covered = np.zeros(N, dtype=np.int64)
     check = set(range(N)) if rows_to_check is None else set(rows_to_check)
@@ -102,7 +102,7 @@ def check_plan_against_oracle(ep, rows_to_check=None):
     assert sorted(slots) == list(range(len(slots))) and len(slots) == st["n_partial_slots"]
     assert sorted(ex["fwd_order"].tolist()) == list(range(len(blocks)))
     # pair count
-    assert st["pairs"] == int((ohi - olo).sum()) == dag.count_pairs(ep.branches, ep.mounts)
+    assert st["pairs"] == int((ohi - olo).sum()) == dag.count_pairs(ep.branches, ep.mounts, view=view)
     assert st["n_rows"] == N
     return plan, ex, st
 
@@ -260,3 +260,46 @@ def test_fwd_rejects_host_only_plan():
     with pytest.raises(ta.TreeAttnError) as ei:
         ta.tree_attn_fwd(plan, 16, 16, 16, 16, 16, stream=0)
     assert ei.value.code == ta.TA_ERR_INVALID
+
+
+# ------------------------------------------------------------------ the two other views
+VIEW_FLAGS = [(ta.TA_NO_MOUNTS, "no_mounts"), (ta.TA_TRANSITIVE_MOUNTS, "transitive")]
+
+
+@pytest.mark.parametrize("flags,view", VIEW_FLAGS, ids=[v for _, v in VIEW_FLAGS])
+@pytest.mark.parametrize("cfg", [0, 2, 4])
+def test_views_full_configs(cfg, flags, view):
+    ep = W.config(cfg)
+    rng = np.random.default_rng(100 + cfg)
+    rows = None if ep.n_rows < 50_000 else rng.choice(ep.n_rows, 2000, replace=False)
+    check_plan_against_oracle(ep, rows, flags=flags, view=view)
+
+
+@pytest.mark.parametrize("flags,view", VIEW_FLAGS, ids=[v for _, v in VIEW_FLAGS])
+@pytest.mark.parametrize("seed", range(24))
+def test_views_random_small(seed, flags, view):
+    ep = W.random_small(500 + seed, max_branches=10, max_len=200, n_mounts=1 + seed % 5)
+    check_plan_against_oracle(ep, flags=flags, view=view)
+
+
+def test_views_crafted_transitive_chain():
+    from test_oracle_views import crafted
+    br, mts = crafted()
+    ep = W.Episode("crafted_views", br, mts, 4, 1, 64, 16, 0)
+    for flags, view in [(0, "mounted")] + VIEW_FLAGS:
+        check_plan_against_oracle(ep, flags=flags, view=view)
+
+
+def test_views_exclusive():
+    ep = W.tiny()
+    with pytest.raises(ta.TreeAttnError):
+        host_plan(ep, flags=ta.TA_NO_MOUNTS | ta.TA_TRANSITIVE_MOUNTS)
+
+
+def test_no_mounts_plan_equals_mount_free_plan_except_positions():
+    ep = W.scaled(4, 64)
+    a = ta.tree_attn_plan_export(host_plan(ep, flags=ta.TA_NO_MOUNTS))
+    b = ta.tree_attn_plan_export(host_plan(ep, mounts=ep.mounts[:0]))
+    for key in ("blocks", "blk_iv_ptr", "iv_lo", "iv_hi", "diag", "entries", "t_entries", "chunks"):
+        assert np.array_equal(a[key], b[key]), key
+    assert np.array_equal(a["pos_ids"], dag.positions(ep.branches, ep.mounts))
