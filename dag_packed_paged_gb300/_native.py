@@ -13,6 +13,10 @@ import numpy as np
 
 from .build import LIB, INCLUDE
 
+# numpy view of ta_branch (int32 parent, fork_offset, length; int64 row_start; C alignment)
+BRANCH_DTYPE = np.dtype(
+    [("parent", "<i4"), ("fork_offset", "<i4"), ("length", "<i4"), ("row_start", "<i8")], align=True)
+
 TA_OK = 0
 TA_ERR_INVALID = -1
 TA_ERR_UNSUPPORTED = -2
@@ -114,6 +118,8 @@ def lib():
     L.tree_attn_plan_destroy.restype = None
     L.tree_attn_set_trace_events.argtypes = [vp, ctypes.POINTER(vp), ctypes.c_int]
     L.tree_attn_set_trace_events.restype = ctypes.c_int
+    L.tree_attn_ingest.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32), vp, i64, ctypes.POINTER(i64), vp]
+    L.tree_attn_ingest.restype = ctypes.c_int
     L.tree_attn_last_error.argtypes = []
     L.tree_attn_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -265,3 +271,25 @@ def tree_attn_plan_destroy(plan: Plan) -> None:
     h, plan.handle = plan.handle, None
     if h:
         lib().tree_attn_plan_destroy(h)
+
+
+def tree_attn_ingest(trajectories):
+    """Compact prefix-tree episode of a list of token trajectories (1-D int arrays).
+
+    Returns (branches, row_tokens, row_of): the ta_branch structured array, the token of every
+    compact row, and for each trajectory the int64 array of compact rows of its positions."""
+    trajs = [np.ascontiguousarray(t, dtype=np.int32).ravel() for t in trajectories]
+    offsets = np.zeros(len(trajs) + 1, dtype=np.int64)
+    for i, t in enumerate(trajs):
+        offsets[i + 1] = offsets[i] + len(t)
+    tokens = np.concatenate(trajs) if trajs and offsets[-1] > 0 else np.zeros(1, dtype=np.int32)
+    total = int(offsets[-1])
+    br = np.zeros(max(len(trajs), 1), dtype=BRANCH_DTYPE)
+    row_tokens = np.zeros(max(total, 1), dtype=np.int32)
+    row_of = np.zeros(max(total, 1), dtype=np.int64)
+    nb, nr = ctypes.c_int32(0), ctypes.c_int64(0)
+    _check(lib().tree_attn_ingest(tokens.ctypes.data, offsets.ctypes.data, len(trajs), br.ctypes.data, len(br),
+                                  ctypes.byref(nb), row_tokens.ctypes.data, len(row_tokens), ctypes.byref(nr),
+                                  row_of.ctypes.data))
+    return br[:nb.value].copy(), row_tokens[:nr.value].copy(), [row_of[offsets[i]:offsets[i + 1]].copy()
+                                                                  for i in range(len(trajs))]

@@ -1,0 +1,101 @@
+// Trajectory ingestion: raw token trajectories -> the compact prefix-tree DAG.
+//
+// HARTS (arXiv 2608.28158) Section 2.1 keeps one compact row per distinct token prefix and a
+// map m: S -> C from every semantic position s = (trajectory, offset) to its compact row
+// (Eq. 3); Section 3.2 counts the rows of a trajectory set as
+//   C(M) = |x_1| + sum_{i >= 2} (|x_i| - LCP(x_{i-1}, x_i))        (Eq. 5)
+// over the trajectories in lexicographic order, where the immediate predecessor gives the
+// longest prefix shared with any trajectory already inserted.  Building the tree in that order
+// gives exactly C(M) rows: each trajectory forks from the branch of its predecessor's path
+// that holds its last shared token, at that token's offset within the branch, and its
+// unshared suffix becomes a new branch.  Branches are laid out in creation order, which is a
+// depth-first order of the prefix tree (every subtree's rows are contiguous).
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#include "plan.h"
+
+namespace treeattn {
+void set_error(const std::string &msg);
+}
+
+using treeattn::set_error;
+
+extern "C" int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, int32_t n_traj,
+                                ta_branch *branches, int32_t max_branches, int32_t *n_branches,
+                                int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of) {
+    if (n_traj < 0 || !offsets || !n_branches || !n_rows || (n_traj > 0 && !row_of)) {
+        set_error("tree_attn_ingest: bad arguments");
+        return TA_ERR_INVALID;
+    }
+    for (int32_t i = 0; i < n_traj; ++i)
+        if (offsets[i + 1] < offsets[i] || offsets[i] < 0) {
+            set_error("tree_attn_ingest: offsets must be non-decreasing from 0");
+            return TA_ERR_INVALID;
+        }
+    const int64_t total = n_traj > 0 ? offsets[n_traj] : 0;
+    if (total > 0 && !tokens) {
+        set_error("tree_attn_ingest: tokens is NULL");
+        return TA_ERR_INVALID;
+    }
+    auto len = [&](int32_t i) { return offsets[i + 1] - offsets[i]; };
+    auto tok = [&](int32_t i) { return tokens + offsets[i]; };
+
+    // lexicographic order (ties keep the input order)
+    std::vector<int32_t> order(n_traj);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+        return std::lexicographical_compare(tok(a), tok(a) + len(a), tok(b), tok(b) + len(b));
+    });
+
+    struct Seg { int32_t branch; int64_t start; };   // a branch on the current path, from offset start
+    std::vector<Seg> path;                           // path of the previous trajectory
+    std::vector<ta_branch> out;
+    int64_t rows = 0;
+    int32_t prev = -1;
+    for (int32_t i : order) {
+        const int64_t n = len(i);
+        int64_t lcp = 0;
+        if (prev >= 0) {
+            const int64_t m = std::min(n, len(prev));
+            const int32_t *a = tok(prev), *b = tok(i);
+            while (lcp < m && a[lcp] == b[lcp]) ++lcp;
+        }
+        // keep the path's branches that hold offsets < lcp; the last one is the fork parent
+        while (!path.empty() && path.back().start >= lcp) path.pop_back();
+        if (n > lcp) {
+            ta_branch br;
+            if (path.empty()) {
+                br.parent = -1;
+                br.fork_offset = 0;
+            } else {
+                br.parent = path.back().branch;
+                br.fork_offset = static_cast<int32_t>(lcp - path.back().start);
+            }
+            br.length = static_cast<int32_t>(n - lcp);
+            br.row_start = rows;
+            if ((int64_t)out.size() >= max_branches || rows + (n - lcp) > max_rows) {
+                set_error("tree_attn_ingest: output capacity too small");
+                return TA_ERR_INVALID;
+            }
+            if (row_tokens) std::memcpy(row_tokens + rows, tok(i) + lcp, sizeof(int32_t) * (n - lcp));
+            rows += n - lcp;
+            out.push_back(br);
+            path.push_back({static_cast<int32_t>(out.size() - 1), lcp});
+        }
+        // the compact row of every offset of trajectory i, along its path
+        for (size_t k = 0; k < path.size(); ++k) {
+            const int64_t a = path[k].start;
+            const int64_t z = k + 1 < path.size() ? path[k + 1].start : n;
+            const ta_branch &b = out[path[k].branch];
+            for (int64_t t = a; t < z && t < n; ++t) row_of[offsets[i] + t] = b.row_start + (t - a);
+        }
+        prev = i;
+    }
+    if (branches) std::copy(out.begin(), out.end(), branches);
+    *n_branches = static_cast<int32_t>(out.size());
+    *n_rows = rows;
+    return TA_OK;
+}

@@ -143,6 +143,33 @@ typedef struct {
     const int32_t *fwd_order;
 } ta_plan_arrays;
 
+/* Build the compact prefix-tree episode of a set of token trajectories.
+ *
+ * HARTS (arXiv 2608.28158) Section 2.1: one compact row per distinct token prefix and a map
+ * m: S -> C from every semantic position (trajectory, offset) to its compact row (Eq. 3);
+ * Section 3.2, Eq. 5: with the trajectories in lexicographic order, the row count is
+ * |x_1| + sum_i (|x_i| - LCP(x_{i-1}, x_i)).  The result has exactly that many rows: each
+ * trajectory forks from the branch of its predecessor's path holding its last shared token,
+ * and its unshared suffix becomes a new branch.  Rows are laid out in creation order (a depth-
+ * first order of the tree).  The branches need no mounts; tree_attn_plan accepts them as is,
+ * and the plan's position ids equal the trajectory offsets.
+ *
+ *   tokens        host, int32[offsets[n_traj]]: the trajectories concatenated
+ *   offsets       host, int64[n_traj + 1]: trajectory i is tokens[offsets[i], offsets[i+1]),
+ *                 non-decreasing from offsets[0] = 0 (empty trajectories allowed)
+ *   branches      host, out, capacity max_branches (n_traj always suffices); may be NULL to
+ *                 query *n_branches only when max_branches >= the count
+ *   row_tokens    host, out, int32[max_rows] (offsets[n_traj] always suffices): the token of
+ *                 every compact row; may be NULL
+ *   n_rows        out: the compact row count (Eq. 5)
+ *   row_of        host, out, int64[offsets[n_traj]]: m, the compact row of every position,
+ *                 in the layout of `tokens`
+ * Returns TA_OK, or TA_ERR_INVALID (bad offsets, NULL arrays, capacity too small).  Pure host
+ * code: no GPU, no allocation visible to the caller. */
+int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, int32_t n_traj,
+                     ta_branch *branches, int32_t max_branches, int32_t *n_branches,
+                     int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of);
+
 /*
  * tree_attn_plan -- validate an episode DAG and build the work plan (host C++).
  *
