@@ -236,6 +236,45 @@ def workload_config(ep, args, stats=None):
     return cfg
 
 
+def run_rope(args, ep):
+    """RoPE of Q and the K pool at the plan's positions, timed alone (HBM-bound): one JSON line
+    with the algorithmic bytes (every Q and K element read and written once) per second."""
+    import torch
+    import dag_packed_paged_gb300 as ta
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    t = W.make_tensors(ep)
+    pool = W.make_pool(ep, t)
+    N, Hq, Hkv, D = ep.n_rows, ep.num_q_heads, ep.num_kv_heads, ep.head_dim
+    plan = ta.tree_attn_plan(ep.branches, ep.mounts, pool.page_table, num_q_heads=Hq, num_kv_heads=Hkv,
+                             head_dim=D, page_size=ep.page_size, num_pages=pool.k_pool.shape[0])
+    q = bf16_dev(t.q, dev)
+    k_pool = bf16_dev(pool.k_pool, dev)
+    for _ in range(args.warmup):
+        ta.tree_attn_rope(plan, q, k_pool, 1e4)
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for _ in range(args.steps):
+        ta.tree_attn_rope(plan, q, k_pool, 1e4)       # inputs (Q + K > L2) stream from HBM each call
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ta.tree_attn_check(plan)
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    nbytes = 2 * N * (Hq + Hkv) * D * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, kind = load_peaks()
+    print(json.dumps({
+        "metric": "rope_hbm_throughput", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": N, "heads": [Hq, Hkv], "head_dim": D},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_kind": f"HBM copy ({kind})",
+                     "algorithmic": f"{nbytes / 1e9:.3f} GB per launch (Q and K read and written once)"},
+        "gpu_launches": args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -245,6 +284,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default="attention", choices=["attention", "rope"],
+                    help="attention: the forward + backward step (the headline); rope: the RoPE kernel alone")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -255,6 +296,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, ep, world, rank)
+        return
+    if args.op == "rope":
+        run_rope(args, ep)
         return
 
     import torch

@@ -118,6 +118,8 @@ def lib():
     L.tree_attn_plan_destroy.restype = None
     L.tree_attn_set_trace_events.argtypes = [vp, ctypes.POINTER(vp), ctypes.c_int]
     L.tree_attn_set_trace_events.restype = ctypes.c_int
+    L.tree_attn_rope.argtypes = [vp, vp, vp, ctypes.c_double, vp]
+    L.tree_attn_rope.restype = ctypes.c_int
     L.tree_attn_ingest.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32), vp, i64, ctypes.POINTER(i64), vp]
     L.tree_attn_ingest.restype = ctypes.c_int
     L.tree_attn_last_error.argtypes = []
@@ -293,3 +295,8 @@ def tree_attn_ingest(trajectories):
                                   row_of.ctypes.data))
     return br[:nb.value].copy(), row_tokens[:nr.value].copy(), [row_of[offsets[i]:offsets[i + 1]].copy()
                                                                   for i in range(len(trajs))]
+
+
+def tree_attn_rope(plan: Plan, q, k_pool, theta_base: float = 10000.0, stream=None) -> None:
+    """Rotate Q [N, Hq, D] and the K pool in place at the plan's Eq. 2 positions."""
+    _check(lib().tree_attn_rope(plan.handle, _ptr(q), _ptr(k_pool), float(theta_base), _stream(stream)))

@@ -134,12 +134,13 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         size_t bytes;
         size_t off;
     };
-    Part parts[10] = {
+    Part parts[11] = {
         {h.blocks.data(), h.blocks.size() * 4, 0},   {h.entries.data(), h.entries.size() * 4, 0},
         {h.t_entries.data(), h.t_entries.size() * 4, 0}, {h.chunks.data(), h.chunks.size() * 4, 0},
         {h.fwd_order.data(), h.fwd_order.size() * 4, 0}, {h.reduce.data(), h.reduce.size() * 4, 0},
         {h.page_table.data(), h.page_table.size() * 4, 0}, {nullptr, 64, 0},
         {h.tile_rows.data(), h.tile_rows.size() * 4, 0}, {h.t_info.data(), h.t_info.size() * 4, 0},
+        {h.pos_ids.data(), h.pos_ids.size() * 4, 0},
     };
     size_t total = 0;
     for (Part &p : parts) {
@@ -178,6 +179,7 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     plan->d_status = reinterpret_cast<int32_t *>(d + parts[7].off);
     plan->d_tile_rows = reinterpret_cast<const int32_t *>(d + parts[8].off);
     plan->d_t_info = reinterpret_cast<const int32_t *>(d + parts[9].off);
+    plan->d_pos_ids = reinterpret_cast<const int32_t *>(d + parts[10].off);
     *out = plan;
     return TA_OK;
 }
@@ -278,6 +280,37 @@ int tree_attn_check(const ta_plan *plan, void *stream) {
         return TA_ERR_CUDA;
     }
     return TA_OK;
+}
+
+int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base, void *stream) {
+    if (!plan) {
+        set_error("plan is NULL");
+        return TA_ERR_INVALID;
+    }
+    const HostPlan &h = plan->host;
+    if (!(theta_base > 1.0) || !std::isfinite(theta_base)) {
+        set_error("tree_attn_rope: theta_base must be a finite number > 1");
+        return TA_ERR_INVALID;
+    }
+    if (h.N == 0) return TA_OK;
+    if (host_only(plan)) return TA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_pool)) {
+        set_error("tree_attn_rope: NULL or misaligned (16-byte) pointer");
+        return TA_ERR_INVALID;
+    }
+    const int D = h.cfg.head_dim;
+    RopeParams p{};
+    p.q = static_cast<__nv_bfloat16 *>(q);
+    p.k_pool = static_cast<__nv_bfloat16 *>(k_pool);
+    p.pos_ids = plan->d_pos_ids;
+    p.page_table = plan->d_page_table;
+    p.N = h.N;
+    p.Hq = h.cfg.num_q_heads;
+    p.Hkv = h.cfg.num_kv_heads;
+    p.page_size = h.cfg.page_size;
+    for (int i = 0; i < D / 2; ++i) p.inv_freq[i] = std::pow(theta_base, -2.0 * i / D);
+    cudaError_t e = launch_rope(D, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : cuda_fail(e, "rope launch");
 }
 
 int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool, void *o,

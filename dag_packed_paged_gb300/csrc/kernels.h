@@ -58,6 +58,19 @@ struct BwdParams {
 };
 
 // `trace`: NULL, or cudaEvent_t handles (entries may be NULL) recorded around the launches.
+// Rotary position embedding of Q and the K pool in place (see rope.cu).
+struct RopeParams {
+    __nv_bfloat16 *q;           // [N, Hq, D]
+    __nv_bfloat16 *k_pool;      // [num_pages * P, Hkv, D]
+    const int32_t *pos_ids;     // [N] Eq. 2 positions
+    const int32_t *page_table;  // logical page -> pool page
+    int64_t N;
+    int32_t Hq, Hkv, page_size;
+    double inv_freq[64];        // theta_base^(-2i/D), i < D/2
+};
+
+cudaError_t launch_rope(int D, const RopeParams &p, cudaStream_t stream);
+
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace);
 

@@ -66,6 +66,7 @@ struct ta_plan {
     const int32_t *d_page_table = nullptr;
     const int32_t *d_tile_rows = nullptr;
     const int32_t *d_t_info = nullptr;
+    const int32_t *d_pos_ids = nullptr;   // Eq. 2 position of every compact row
     int32_t *d_status = nullptr;      // bounded-wait status words (zeroed at plan time)
     size_t ws_table_bytes = 0;        // workspace: per (KV head, block, query tile) 128 lse*log2e + 128 delta
     size_t ws_bytes = 0;              // total bwd workspace

@@ -203,6 +203,22 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
                    int32_t n_mounts, const int32_t *page_table, int64_t n_logical_pages,
                    const ta_config *config, int32_t *pos_ids_out, void *stream, ta_plan **out);
 
+/* Rotary position embedding of Q and the K pool, in place, at the plan's Eq. 2 positions.
+ *
+ * Octopus (arXiv 2611.06956) Section 3.2: scores see positions only through the rotary phase
+ * relation <R_p q, R_s k> = <q, R_{s-p} k> (Eq. 1), which is why mounted spans keep their own
+ * positions and readers continue after them (Eq. 2); HARTS (arXiv 2608.28158) Section 4.2
+ * applies RoPE once per compact row before attention.  Pair layout (a reading: the pages give
+ * only Eq. 1): element i and i + D/2 of every head vector are rotated by p * theta_i,
+ * theta_i = theta_base^(-2i/D), i < D/2, p = pos_ids[row].
+ *
+ *   q       device, bf16 [N, num_q_heads, head_dim], compact rows; rotated in place
+ *   k_pool  device, bf16 [num_pages, page_size, num_kv_heads, head_dim]; the rows the page
+ *           table maps are rotated in place, spare pages are not touched (V is not rotated)
+ *   theta_base  > 1 (10000 in the original RoPE; model-specific)
+ * One kernel on `stream`, HBM-bound; TA_ERR_INVALID for bad arguments or a host-only plan. */
+int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base, void *stream);
+
 /*
  * tree_attn_fwd -- O and logsumexp of every compact row (device, sm_103a).
  *
