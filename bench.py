@@ -275,6 +275,67 @@ def run_rope(args, ep):
         "gpu_launches": args.steps}))
 
 
+def run_logprob(args, ep, vocab=151_936):
+    """Compact-to-semantic log-probabilities (forward + backward) over the episode's compact rows
+    with a 151,936-token vocabulary; HBM-bound: the logits are read once forward, read once and
+    the logit gradient written once backward."""
+    import torch
+    import dag_packed_paged_gb300 as ta
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    C = ep.n_rows
+    pr, pt, _ = W.semantic_positions(ep, vocab, seed=ep.seed)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(ep.seed + 17)
+    z = (torch.randn((C, vocab), generator=gen, device=dev) * 3.0).to(torch.bfloat16)
+    g = torch.randn(len(pr), generator=gen, device=dev)
+    pos_row = torch.from_numpy(pr).to(dev)
+    pos_tgt = torch.from_numpy(pt).to(dev)
+    ptr_h, pos_h = ta.tree_attn_logprob_index(pr, pt, C, vocab)
+    row_ptr, row_pos = torch.from_numpy(ptr_h).to(dev), torch.from_numpy(pos_h).to(dev)
+    lse = torch.empty(C, dtype=torch.float32, device=dev)
+    lp = torch.empty(len(pr), dtype=torch.float32, device=dev)
+    dz = torch.empty_like(z)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        ta.tree_attn_logprob_fwd(z, pos_row, pos_tgt, lse, lp)
+
+    def bwd():
+        ta.tree_attn_logprob_bwd(z, lse, row_ptr, row_pos, pos_tgt, g, dz)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    fwd_ms = bwd_ms = 0.0
+    for _ in range(args.steps):                   # logits (13.7 GB at the default) >> L2
+        ev[0].record(stream)
+        fwd()
+        ev[1].record(stream)
+        bwd()
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        fwd_ms += ev[0].elapsed_time(ev[1])
+        bwd_ms += ev[1].elapsed_time(ev[2])
+    fwd_ms /= args.steps
+    bwd_ms /= args.steps
+    fwd_bytes, bwd_bytes = C * vocab * 2, 2 * C * vocab * 2
+    gbs = (fwd_bytes + bwd_bytes) / ((fwd_ms + bwd_ms) * 1e-3) / 1e9
+    peaks, kind = load_peaks()
+    print(json.dumps({
+        "metric": "logprob_hbm_throughput", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": fwd_ms + bwd_ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "compact_rows": C, "semantic_positions": int(len(pr)), "vocab": vocab},
+        "kernel_ms": {"fwd": fwd_ms, "bwd": bwd_ms},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_kind": f"HBM copy ({kind})",
+                     "algorithmic": f"{fwd_bytes / 1e9:.2f} GB forward + {bwd_bytes / 1e9:.2f} GB backward"},
+        "gpu_launches": 3 * args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -284,8 +345,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="attention", choices=["attention", "rope"],
-                    help="attention: the forward + backward step (the headline); rope: the RoPE kernel alone")
+    ap.add_argument("--op", default="attention", choices=["attention", "rope", "logprob"],
+                    help="attention: the forward + backward step (the headline); rope: the RoPE kernel alone; "
+                         "logprob: compact log-probabilities forward + backward (vocabulary 151,936)")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -299,6 +361,9 @@ def main():
         return
     if args.op == "rope":
         run_rope(args, ep)
+        return
+    if args.op == "logprob":
+        run_logprob(args, ep)
         return
 
     import torch

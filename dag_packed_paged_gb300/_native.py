@@ -118,6 +118,12 @@ def lib():
     L.tree_attn_plan_destroy.restype = None
     L.tree_attn_set_trace_events.argtypes = [vp, ctypes.POINTER(vp), ctypes.c_int]
     L.tree_attn_set_trace_events.restype = ctypes.c_int
+    L.tree_attn_logprob_fwd.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp]
+    L.tree_attn_logprob_fwd.restype = ctypes.c_int
+    L.tree_attn_logprob_bwd.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+    L.tree_attn_logprob_bwd.restype = ctypes.c_int
+    L.tree_attn_logprob_index.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+    L.tree_attn_logprob_index.restype = ctypes.c_int
     L.tree_attn_rope.argtypes = [vp, vp, vp, ctypes.c_double, vp]
     L.tree_attn_rope.restype = ctypes.c_int
     L.tree_attn_ingest.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32), vp, i64, ctypes.POINTER(i64), vp]
@@ -300,3 +306,30 @@ def tree_attn_ingest(trajectories):
 def tree_attn_rope(plan: Plan, q, k_pool, theta_base: float = 10000.0, stream=None) -> None:
     """Rotate Q [N, Hq, D] and the K pool in place at the plan's Eq. 2 positions."""
     _check(lib().tree_attn_rope(plan.handle, _ptr(q), _ptr(k_pool), float(theta_base), _stream(stream)))
+
+
+def tree_attn_logprob_fwd(logits, pos_row, pos_target, row_lse, logprob, stream=None) -> None:
+    """logits bf16 [C, V]; pos_row int64 [S]; pos_target int32 [S] (device tensors) ->
+    row_lse fp32 [C], logprob fp32 [S]."""
+    C, V = logits.shape
+    _check(lib().tree_attn_logprob_fwd(_ptr(logits), C, V, _ptr(pos_row), _ptr(pos_target), pos_row.shape[0],
+                                       _ptr(row_lse), _ptr(logprob), _stream(stream)))
+
+
+def tree_attn_logprob_index(pos_row: np.ndarray, pos_target: np.ndarray, n_rows: int, vocab: int):
+    """Host CSR of the positions of every compact row, ordered by target: (row_ptr, row_pos)."""
+    pr = np.ascontiguousarray(pos_row, dtype=np.int64)
+    pt = np.ascontiguousarray(pos_target, dtype=np.int32)
+    row_ptr = np.zeros(n_rows + 1, dtype=np.int64)
+    row_pos = np.zeros(max(len(pr), 1), dtype=np.int64)
+    _check(lib().tree_attn_logprob_index(pr.ctypes.data if len(pr) else None, pt.ctypes.data if len(pt) else None,
+                                         len(pr), n_rows, vocab, row_ptr.ctypes.data, row_pos.ctypes.data))
+    return row_ptr, row_pos[: len(pr)]
+
+
+def tree_attn_logprob_bwd(logits, row_lse, row_ptr, row_pos, pos_target, dlogprob, dlogits, stream=None) -> None:
+    """dlogits bf16 [C, V] from dlogprob fp32 [S] (device tensors; row_ptr / row_pos from
+    tree_attn_logprob_index, moved to the device)."""
+    C, V = logits.shape
+    _check(lib().tree_attn_logprob_bwd(_ptr(logits), C, V, _ptr(row_lse), _ptr(row_ptr), _ptr(row_pos),
+                                       _ptr(pos_target), _ptr(dlogprob), _ptr(dlogits), _stream(stream)))

@@ -282,6 +282,47 @@ int tree_attn_check(const ta_plan *plan, void *stream) {
     return TA_OK;
 }
 
+int tree_attn_logprob_fwd(const void *logits, int64_t n_rows, int64_t vocab, const int64_t *pos_row,
+                          const int32_t *pos_target, int64_t n_pos, float *row_lse, float *logprob, void *stream) {
+    if (n_rows < 0 || n_pos < 0 || vocab <= 0 || vocab > INT32_MAX) {
+        set_error("tree_attn_logprob_fwd: bad sizes");
+        return TA_ERR_INVALID;
+    }
+    if (vocab % 8) {
+        set_error("tree_attn_logprob_fwd: vocab must be a multiple of 8");
+        return TA_ERR_UNSUPPORTED;
+    }
+    if ((n_rows > 0 && (!aligned16(logits) || !row_lse)) || (n_pos > 0 && (!pos_row || !pos_target || !logprob))) {
+        set_error("tree_attn_logprob_fwd: NULL or misaligned (16-byte) pointer");
+        return TA_ERR_INVALID;
+    }
+    cudaError_t e = launch_logprob_fwd(static_cast<const __nv_bfloat16 *>(logits), n_rows, vocab, pos_row, pos_target,
+                                       n_pos, row_lse, logprob, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : cuda_fail(e, "logprob forward launch");
+}
+
+int tree_attn_logprob_bwd(const void *logits, int64_t n_rows, int64_t vocab, const float *row_lse,
+                          const int64_t *row_ptr, const int64_t *row_pos, const int32_t *pos_target,
+                          const float *dlogprob, void *dlogits, void *stream) {
+    if (n_rows < 0 || vocab <= 0 || vocab > INT32_MAX) {
+        set_error("tree_attn_logprob_bwd: bad sizes");
+        return TA_ERR_INVALID;
+    }
+    if (vocab % 8) {
+        set_error("tree_attn_logprob_bwd: vocab must be a multiple of 8");
+        return TA_ERR_UNSUPPORTED;
+    }
+    if (n_rows > 0 && (!aligned16(logits) || !aligned16(dlogits) || !row_lse || !row_ptr || !row_pos ||
+                       !pos_target || !dlogprob)) {
+        set_error("tree_attn_logprob_bwd: NULL or misaligned (16-byte) pointer");
+        return TA_ERR_INVALID;
+    }
+    cudaError_t e = launch_logprob_bwd(static_cast<const __nv_bfloat16 *>(logits), n_rows, vocab, row_lse, row_ptr,
+                                       row_pos, pos_target, dlogprob, static_cast<__nv_bfloat16 *>(dlogits),
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : cuda_fail(e, "logprob backward launch");
+}
+
 int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base, void *stream) {
     if (!plan) {
         set_error("plan is NULL");

@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cstring>
 #include <numeric>
+#include <string>
 #include <vector>
 
 #include "plan.h"
@@ -97,5 +98,32 @@ extern "C" int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, i
     if (branches) std::copy(out.begin(), out.end(), branches);
     *n_branches = static_cast<int32_t>(out.size());
     *n_rows = rows;
+    return TA_OK;
+}
+
+// The positions of every compact row, for the backward of the compact log-probabilities: a
+// CSR (row_ptr[C + 1], row_pos[S]) of the semantic positions grouped by compact row and, within
+// a row, ordered by target token (then by position), so that positions sharing a target are
+// adjacent and the kernel sums their gradients in a fixed order.
+extern "C" int tree_attn_logprob_index(const int64_t *pos_row, const int32_t *pos_target, int64_t n_pos,
+                                       int64_t n_rows, int64_t vocab, int64_t *row_ptr, int64_t *row_pos) {
+    if (n_pos < 0 || n_rows < 0 || vocab <= 0 || !row_ptr || (n_pos > 0 && (!pos_row || !pos_target || !row_pos))) {
+        set_error("tree_attn_logprob_index: bad arguments");
+        return TA_ERR_INVALID;
+    }
+    std::fill(row_ptr, row_ptr + n_rows + 1, 0);
+    for (int64_t s = 0; s < n_pos; ++s) {
+        if (pos_row[s] < 0 || pos_row[s] >= n_rows || pos_target[s] < 0 || pos_target[s] >= vocab) {
+            set_error("tree_attn_logprob_index: position " + std::to_string(s) + " has a row or target out of range");
+            return TA_ERR_INVALID;
+        }
+        ++row_ptr[pos_row[s] + 1];
+    }
+    for (int64_t c = 0; c < n_rows; ++c) row_ptr[c + 1] += row_ptr[c];
+    std::vector<int64_t> fill(row_ptr, row_ptr + n_rows);
+    for (int64_t s = 0; s < n_pos; ++s) row_pos[fill[pos_row[s]]++] = s;
+    for (int64_t c = 0; c < n_rows; ++c)
+        std::stable_sort(row_pos + row_ptr[c], row_pos + row_ptr[c + 1],
+                         [&](int64_t a, int64_t b) { return pos_target[a] < pos_target[b]; });
     return TA_OK;
 }

@@ -71,6 +71,13 @@ struct RopeParams {
 
 cudaError_t launch_rope(int D, const RopeParams &p, cudaStream_t stream);
 
+// Compact-to-semantic log-probabilities (see logprob.cu).
+cudaError_t launch_logprob_fwd(const __nv_bfloat16 *z, int64_t C, int64_t V, const int64_t *pos_row,
+                               const int32_t *pos_target, int64_t S, float *lse, float *logprob, cudaStream_t stream);
+cudaError_t launch_logprob_bwd(const __nv_bfloat16 *z, int64_t C, int64_t V, const float *lse, const int64_t *row_ptr,
+                               const int64_t *row_pos, const int32_t *pos_target, const float *g, __nv_bfloat16 *dz,
+                               cudaStream_t stream);
+
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace);
 

@@ -415,3 +415,31 @@ def pool_rows(pool_arr: np.ndarray, page_table: np.ndarray, n_rows: int) -> np.n
     P = pool_arr.shape[1]
     g = pool_arr[page_table]
     return g.reshape((g.shape[0] * P,) + pool_arr.shape[2:])[:n_rows]
+
+
+def semantic_positions(ep: Episode, vocab: int, seed: int = 0):
+    """Semantic positions of an episode for the compact log-probabilities (HARTS Section 4): one
+    trajectory per branch (its root-to-end path of compact rows; mounted spans are keys only and
+    carry no positions), every non-final position of it predicting the token of the next row.
+    Compact rows get seeded random tokens in [0, vocab).  Returns (pos_row int64[S],
+    pos_target int32[S], row_token int32[N])."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 3003]))
+    br = ep.branches
+    row_token = rng.integers(0, vocab, size=ep.n_rows).astype(np.int32)
+    rows_all, tgt_all = [], []
+    for b in range(len(br)):
+        segs = []
+        x, hi = b, int(br["length"][b])
+        while x >= 0:
+            rs = int(br["row_start"][x])
+            segs.append(np.arange(rs, rs + hi, dtype=np.int64))
+            p = int(br["parent"][x])
+            hi = int(br["fork_offset"][x])
+            x = p
+        path = np.concatenate(segs[::-1])
+        if len(path) > 1:
+            rows_all.append(path[:-1])
+            tgt_all.append(row_token[path[1:]])
+    if not rows_all:
+        return np.zeros(0, np.int64), np.zeros(0, np.int32), row_token
+    return np.concatenate(rows_all), np.concatenate(tgt_all).astype(np.int32), row_token

@@ -219,6 +219,38 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
  * One kernel on `stream`, HBM-bound; TA_ERR_INVALID for bad arguments or a host-only plan. */
 int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base, void *stream);
 
+/* Compact-to-semantic log-probabilities (HARTS, arXiv 2608.28158, Section 4).
+ *
+ * A compact row c's LM-head logits z_c serve every semantic position s with m(s) = c (the map
+ * of tree_attn_ingest).  Eq. 17: lambda_s = z_{m(s), y_s} - log sum_v exp z_{m(s), v}, the
+ * vocabulary-wide maximum and sum-exp formed once per compact row; Eq. 19-20: the backward
+ * accumulates every position's gradient into its row, dz_c = sum_{m(s)=c} g_s (e_{y_s} -
+ * softmax(z_c)).  Nothing of size positions x vocab is formed.
+ *
+ *   logits     device, bf16 [n_rows, vocab] row-major, 16-byte aligned; vocab a multiple of 8
+ *              (TA_ERR_UNSUPPORTED otherwise)
+ *   pos_row    device, int64 [n_pos]: m(s), the compact row of position s
+ *   pos_target device, int32 [n_pos]: y_s, the next token of position s
+ *   row_lse    device, fp32 [n_rows], out (fwd) / in (bwd): natural-log sum-exp of every row
+ *   logprob    device, fp32 [n_pos], out: lambda_s in the caller's order (NaN for a position
+ *              whose row or target is out of range)
+ *   row_ptr, row_pos  device, int64 [n_rows + 1], [n_pos]: the positions of each row, ordered by
+ *              target, as built by tree_attn_logprob_index (host)
+ *   dlogprob   device, fp32 [n_pos]: g_s = dL/dlambda_s (0 for positions outside the action mask)
+ *   dlogits    device, bf16 [n_rows, vocab], out, 16-byte aligned; every element written once
+ *              (rows no position reads are 0); deterministic
+ * Each call enqueues its kernels on `stream` (forward: 2, backward: 1); HBM-bound.  Returns
+ * TA_OK, TA_ERR_INVALID or TA_ERR_UNSUPPORTED (arguments), TA_ERR_CUDA (launch). */
+int tree_attn_logprob_fwd(const void *logits, int64_t n_rows, int64_t vocab, const int64_t *pos_row,
+                          const int32_t *pos_target, int64_t n_pos, float *row_lse, float *logprob, void *stream);
+int tree_attn_logprob_bwd(const void *logits, int64_t n_rows, int64_t vocab, const float *row_lse,
+                          const int64_t *row_ptr, const int64_t *row_pos, const int32_t *pos_target,
+                          const float *dlogprob, void *dlogits, void *stream);
+/* Host: the CSR row_ptr[n_rows + 1] / row_pos[n_pos] that tree_attn_logprob_bwd reads, from
+ * host copies of pos_row and pos_target; TA_ERR_INVALID if a row or target is out of range. */
+int tree_attn_logprob_index(const int64_t *pos_row, const int32_t *pos_target, int64_t n_pos,
+                            int64_t n_rows, int64_t vocab, int64_t *row_ptr, int64_t *row_pos);
+
 /*
  * tree_attn_fwd -- O and logsumexp of every compact row (device, sm_103a).
  *
