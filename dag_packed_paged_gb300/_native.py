@@ -126,7 +126,9 @@ def lib():
     L.tree_attn_logprob_index.restype = ctypes.c_int
     L.tree_attn_rope.argtypes = [vp, vp, vp, ctypes.c_double, vp]
     L.tree_attn_rope.restype = ctypes.c_int
-    L.tree_attn_ingest.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32), vp, i64, ctypes.POINTER(i64), vp]
+    L.tree_attn_ingest.argtypes = [vp, vp, i32, vp, i32, ctypes.POINTER(i32), vp, i64, ctypes.POINTER(i64), vp, vp]
+    L.tree_attn_owner_mask.argtypes = [vp, i32, vp, vp, vp, vp]
+    L.tree_attn_owner_mask.restype = ctypes.c_int
     L.tree_attn_ingest.restype = ctypes.c_int
     L.tree_attn_last_error.argtypes = []
     L.tree_attn_last_error.restype = ctypes.c_char_p
@@ -281,11 +283,12 @@ def tree_attn_plan_destroy(plan: Plan) -> None:
         lib().tree_attn_plan_destroy(h)
 
 
-def tree_attn_ingest(trajectories):
+def tree_attn_ingest(trajectories, with_owner=False):
     """Compact prefix-tree episode of a list of token trajectories (1-D int arrays).
 
     Returns (branches, row_tokens, row_of): the ta_branch structured array, the token of every
-    compact row, and for each trajectory the int64 array of compact rows of its positions."""
+    compact row, and for each trajectory the int64 array of compact rows of its positions;
+    with_owner=True appends row_owner (the trajectory whose insertion created each row)."""
     trajs = [np.ascontiguousarray(t, dtype=np.int32).ravel() for t in trajectories]
     offsets = np.zeros(len(trajs) + 1, dtype=np.int64)
     for i, t in enumerate(trajs):
@@ -295,12 +298,33 @@ def tree_attn_ingest(trajectories):
     br = np.zeros(max(len(trajs), 1), dtype=BRANCH_DTYPE)
     row_tokens = np.zeros(max(total, 1), dtype=np.int32)
     row_of = np.zeros(max(total, 1), dtype=np.int64)
+    row_owner = np.zeros(max(total, 1), dtype=np.int32)
     nb, nr = ctypes.c_int32(0), ctypes.c_int64(0)
     _check(lib().tree_attn_ingest(tokens.ctypes.data, offsets.ctypes.data, len(trajs), br.ctypes.data, len(br),
                                   ctypes.byref(nb), row_tokens.ctypes.data, len(row_tokens), ctypes.byref(nr),
-                                  row_of.ctypes.data))
-    return br[:nb.value].copy(), row_tokens[:nr.value].copy(), [row_of[offsets[i]:offsets[i + 1]].copy()
-                                                                  for i in range(len(trajs))]
+                                  row_of.ctypes.data, row_owner.ctypes.data))
+    out = (br[:nb.value].copy(), row_tokens[:nr.value].copy(), [row_of[offsets[i]:offsets[i + 1]].copy()
+                                                                 for i in range(len(trajs))])
+    return out + (row_owner[:nr.value].copy(),) if with_owner else out
+
+
+def tree_attn_owner_mask(row_of, row_owner, generated=None) -> list:
+    """Octopus Eq. 6 loss mask per trajectory position (list of uint8 arrays, the layout of
+    tree_attn_ingest's row_of): 1 where the position's predicted token is generated and its
+    compact row is owned by this trajectory."""
+    lens = [len(r) for r in row_of]
+    offsets = np.zeros(len(lens) + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(lens)
+    flat = np.concatenate(row_of).astype(np.int64) if offsets[-1] else np.zeros(1, np.int64)
+    own = np.ascontiguousarray(row_owner, dtype=np.int32)
+    gen = None
+    if generated is not None:
+        gen = np.concatenate([np.asarray(g, dtype=np.uint8) for g in generated]) if offsets[-1] else np.zeros(1, np.uint8)
+    mask = np.zeros(max(int(offsets[-1]), 1), dtype=np.uint8)
+    _check(lib().tree_attn_owner_mask(offsets.ctypes.data, len(lens), flat.ctypes.data,
+                                      own.ctypes.data if len(own) else None,
+                                      gen.ctypes.data if gen is not None else None, mask.ctypes.data))
+    return [mask[offsets[i]:offsets[i + 1]].copy() for i in range(len(lens))]
 
 
 def tree_attn_rope(plan: Plan, q, k_pool, theta_base: float = 10000.0, stream=None) -> None:

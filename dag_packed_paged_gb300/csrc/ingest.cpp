@@ -26,7 +26,8 @@ using treeattn::set_error;
 
 extern "C" int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, int32_t n_traj,
                                 ta_branch *branches, int32_t max_branches, int32_t *n_branches,
-                                int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of) {
+                                int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of,
+                                int32_t *row_owner) {
     if (n_traj < 0 || !offsets || !n_branches || !n_rows || (n_traj > 0 && !row_of)) {
         set_error("tree_attn_ingest: bad arguments");
         return TA_ERR_INVALID;
@@ -82,6 +83,7 @@ extern "C" int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, i
                 return TA_ERR_INVALID;
             }
             if (row_tokens) std::memcpy(row_tokens + rows, tok(i) + lcp, sizeof(int32_t) * (n - lcp));
+            if (row_owner) std::fill(row_owner + rows, row_owner + rows + (n - lcp), i);
             rows += n - lcp;
             out.push_back(br);
             path.push_back({static_cast<int32_t>(out.size() - 1), lcp});
@@ -125,5 +127,33 @@ extern "C" int tree_attn_logprob_index(const int64_t *pos_row, const int32_t *po
     for (int64_t c = 0; c < n_rows; ++c)
         std::stable_sort(row_pos + row_ptr[c], row_pos + row_ptr[c + 1],
                          [&](int64_t a, int64_t b) { return pos_target[a] < pos_target[b]; });
+    return TA_OK;
+}
+
+// Octopus (arXiv 2611.06956) Section 3.4, Eq. 6: a prefix-deduplicating loss mask that counts
+// every generated token of the packed strip once, at the trajectory that owns its node, so that
+// summing masked token log-probabilities over all trajectories gives the episode's score
+// function (Eq. 7).  Position (l, t) of trajectory l (t < |l| - 1) predicts token t + 1 from the
+// prefix ending at t; two positions predict the same thing exactly when their predicted tokens
+// share a compact row, so the mask is 1 iff l owns that row (row_owner, from tree_attn_ingest:
+// the trajectory whose insertion created the row) and the predicted token is generated.
+// mask has the layout of `tokens`; the last entry of every trajectory is 0 (no next token).
+extern "C" int tree_attn_owner_mask(const int64_t *offsets, int32_t n_traj, const int64_t *row_of,
+                                    const int32_t *row_owner, const uint8_t *generated, uint8_t *mask) {
+    if (n_traj < 0 || !offsets || (n_traj > 0 && (!row_of || !row_owner || !mask))) {
+        set_error("tree_attn_owner_mask: bad arguments");
+        return TA_ERR_INVALID;
+    }
+    for (int32_t l = 0; l < n_traj; ++l) {
+        const int64_t a = offsets[l], z = offsets[l + 1];
+        if (z < a) {
+            set_error("tree_attn_owner_mask: offsets must be non-decreasing");
+            return TA_ERR_INVALID;
+        }
+        for (int64_t k = a; k < z; ++k) {
+            const bool has_next = k + 1 < z;
+            mask[k] = has_next && row_owner[row_of[k + 1]] == l && (!generated || generated[k + 1]) ? 1 : 0;
+        }
+    }
     return TA_OK;
 }

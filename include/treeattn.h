@@ -164,11 +164,26 @@ typedef struct {
  *   n_rows        out: the compact row count (Eq. 5)
  *   row_of        host, out, int64[offsets[n_traj]]: m, the compact row of every position,
  *                 in the layout of `tokens`
+ *   row_owner     host, out, int32[max_rows], may be NULL: the trajectory (input index) whose
+ *                 insertion created each compact row
  * Returns TA_OK, or TA_ERR_INVALID (bad offsets, NULL arrays, capacity too small).  Pure host
  * code: no GPU, no allocation visible to the caller. */
 int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, int32_t n_traj,
                      ta_branch *branches, int32_t max_branches, int32_t *n_branches,
-                     int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of);
+                     int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of,
+                     int32_t *row_owner);
+
+/* Prefix-deduplicating loss mask (Octopus, arXiv 2611.06956, Section 3.4, Eq. 6): every
+ * generated token of the packed strip is counted once, at the trajectory owning its node, so
+ * that the masked sum of token log-probabilities over all trajectories is the episode's score
+ * function (Eq. 7).  Position k = offsets[l] + t predicts token t + 1 of trajectory l; mask[k]
+ * = 1 iff l owns the compact row of that token (row_owner from tree_attn_ingest) and
+ * generated[k + 1] (NULL: every token counts); the last position of each trajectory is 0.
+ * All arrays host, in the layout of `tokens` (row_owner: per compact row).  Returns TA_OK or
+ * TA_ERR_INVALID.  (The pages do not say which trajectory owns a shared node; here it is the
+ * one whose insertion created the row: the lexicographically first, input order on ties.) */
+int tree_attn_owner_mask(const int64_t *offsets, int32_t n_traj, const int64_t *row_of,
+                         const int32_t *row_owner, const uint8_t *generated, uint8_t *mask);
 
 /*
  * tree_attn_plan -- validate an episode DAG and build the work plan (host C++).

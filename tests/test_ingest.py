@@ -104,9 +104,42 @@ def test_ingest_rejects_bad_arguments():
     out = np.zeros(4, dtype=ta._native.BRANCH_DTYPE)
     rows = np.zeros(4, dtype=np.int64)
     rc = L.tree_attn_ingest(tok.ctypes.data, bad.ctypes.data, 2, out.ctypes.data, 4, ctypes.byref(nb), None, 4,
-                            ctypes.byref(nr), rows.ctypes.data)
+                            ctypes.byref(nr), rows.ctypes.data, None)
     assert rc == ta.TA_ERR_INVALID
     good = np.array([0, 3], dtype=np.int64)
     rc = L.tree_attn_ingest(tok.ctypes.data, good.ctypes.data, 1, out.ctypes.data, 0, ctypes.byref(nb), None, 4,
-                            ctypes.byref(nr), rows.ctypes.data)          # no branch capacity
+                            ctypes.byref(nr), rows.ctypes.data, None)    # no branch capacity
     assert rc == ta.TA_ERR_INVALID
+
+
+# ------------------------------------------------------------------ Octopus Eq. 6 owner mask
+def _prefix_value(prefix):
+    """A deterministic stand-in for log p(last token | rest) of a raw token prefix."""
+    return (hash(tuple(int(x) for x in prefix)) % 10007) / 10007.0 - 0.5
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_owner_mask_counts_every_generated_prefix_once(seed):
+    """Eq. 7: the masked sum over all trajectories' positions equals the sum over the distinct
+    generated token prefixes (each counted once) -- checked against raw token tuples."""
+    trajs = random_trajectories(seed)
+    br, row_tokens, row_of, row_owner = ta.tree_attn_ingest(trajs, with_owner=True)
+    # generated flag as a function of the raw prefix ending at the token (consistent across
+    # trajectories sharing it): prompts / tool outputs are the other tokens
+    generated = [np.array([hash(tuple(int(x) for x in t[: k + 1])) % 3 != 0 for k in range(len(t))], dtype=np.uint8)
+                 for t in trajs]
+    mask = ta.tree_attn_owner_mask(row_of, row_owner, generated)
+    got = sum(_prefix_value(t[: k + 2]) for t, m in zip(trajs, mask) for k in np.nonzero(m)[0])
+    distinct = {tuple(int(x) for x in t[: k + 1]) for t, g in zip(trajs, generated) for k in range(1, len(t)) if g[k]}
+    want = sum(_prefix_value(p) for p in distinct)
+    assert abs(got - want) < 1e-9
+    assert sum(int(m.sum()) for m in mask) == len(distinct)
+    # every masked position sits in the trajectory that owns the predicted token's row
+    for l, (rows, m) in enumerate(zip(row_of, mask)):
+        for k in np.nonzero(m)[0]:
+            assert row_owner[rows[k + 1]] == l
+        if len(m):
+            assert m[-1] == 0
+    # owners pass through the rows they own
+    for c, l in enumerate(row_owner):
+        assert c in set(row_of[l].tolist())
