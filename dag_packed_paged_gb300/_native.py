@@ -110,6 +110,8 @@ def lib():
     L.tree_attn_bwd_workspace_size.restype = sz
     L.tree_attn_check.argtypes = [vp, vp]
     L.tree_attn_check.restype = ctypes.c_int
+    L.tree_attn_selftest_timeout.argtypes = [vp, i64, vp]
+    L.tree_attn_selftest_timeout.restype = ctypes.c_int
     L.tree_attn_plan_stats.argtypes = [vp, ctypes.POINTER(ta_plan_stats)]
     L.tree_attn_plan_stats.restype = ctypes.c_int
     L.tree_attn_plan_export.argtypes = [vp, ctypes.POINTER(ta_plan_arrays)]
@@ -233,6 +235,12 @@ def tree_attn_bwd_workspace_size(plan: Plan) -> int:
 
 def tree_attn_check(plan: Plan, stream=None) -> None:
     _check(lib().tree_attn_check(plan.handle, _stream(stream)))
+
+
+def tree_attn_selftest_timeout(plan: Plan, limit_us: int = 1000, stream=None) -> None:
+    """Launch the kernel whose bounded wait always expires (see include/treeattn.h); the next
+    tree_attn_check on `plan` raises with TA_ERR_DEVICE_TIMEOUT."""
+    _check(lib().tree_attn_selftest_timeout(plan.handle, int(limit_us), _stream(stream)))
 
 
 def tree_attn_set_trace_events(plan: Plan, events) -> None:

@@ -58,21 +58,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  Returns false (and sets
 // *abort and the status word) if it did not complete in kWaitNs, or -- when `abort` is not
 // NULL -- as soon as another thread of the CTA has aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *status) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
+                                              unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (abort != nullptr && *abort) return false;
-            if (globaltimer() - t0 > kWaitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 if (abort != nullptr) *abort = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int *status) {
+    return mbar_wait_for(bar, parity, abort, status, kWaitNs);
 }
 
 // ------------------------------------------------------------------------------ TMA

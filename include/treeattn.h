@@ -344,6 +344,16 @@ size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
  * (TA_ERR_CUDA); clears the status. */
 int tree_attn_check(const ta_plan *plan, void *stream);
 
+/* Diagnostic: runs the bounded-wait error path on purpose.  Launches one kernel on `stream`
+ * in which a single thread waits, for limit_us microseconds (100 .. 1,000,000), on a
+ * shared-memory mbarrier that nothing arrives on; the wait expires, the kernel sets this
+ * plan's timeout status bit exactly as the attention kernels do when a wait of theirs runs
+ * out, and returns normally.  The next tree_attn_check on the plan returns
+ * TA_ERR_DEVICE_TIMEOUT and clears the status; the CUDA context stays usable.  Returns
+ * TA_ERR_INVALID for a NULL or host-only plan or a limit outside the range, TA_ERR_CUDA for a
+ * launch failure. */
+int tree_attn_selftest_timeout(const ta_plan *plan, int64_t limit_us, void *stream);
+
 /* Optional per-kernel tracing.  With events set, tree_attn_fwd records events[0] before and
  * events[1] after its kernel; tree_attn_bwd records events[2], [3], [4], [5] before its
  * delta, dQ, dK/dV and reduce kernels and events[6] after the last one -- all on the call's
