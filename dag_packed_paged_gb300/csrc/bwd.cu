@@ -88,7 +88,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t 
     }
 }
 
-constexpr int kBwdThreads = 320;   // warps 0-3 / 4-7: elementwise groups, 8 loads, 9 MMA
+constexpr int kDqThreads = 352;    // dQ: warps 0-3 / 4-7 elementwise groups, 8 loads, 9 and 10 MMA
 constexpr int kDkvThreads = 352;   // dK/dV: warps 9 and 10 each issue one of the two MMA chains
 constexpr int kQStages = 3;        // dK/dV: Q stages (a Q tile is last read by dK)
 constexpr int kDoStages = 2;       // dK/dV: dO stages (a dO tile is last read by dV)
@@ -119,12 +119,25 @@ __device__ __forceinline__ void issue_acc_split(uint32_t d_tmem, uint32_t a_base
                b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
-// Copy one bf16 row of D elements from global memory into this thread's TMEM lane at
-// column `col` (two elements per 32-bit column, the layout tcgen05.mma reads A from).
+// D[128 x N] (+)= A[128 x 128] * B[128 x N], A in bf16 TMEM columns [a_base, a_base + 64)
+// (K-column k in column a_base + k / 2), B the rows of an MN-major smem tile.
+__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_base, uint32_t sB, uint32_t idesc, bool acc) {
+    const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
+#pragma unroll
+    for (int kk = 0; kk < kTileRows / 16; ++kk)
+        mma_ts(d_tmem, a_base + kk * 8, b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
+               (acc || kk > 0) ? 1u : 0u);
+}
+
+// Copy the 64-element chunks c = w, w + 2, ... of one bf16 row of D elements from global
+// memory into this thread's TMEM lane (chunk c at column `taddr + 32 c`, two elements per
+// 32-bit column: the layout tcgen05.mma reads A from).  The two elementwise groups (w = 0, 1)
+// each copy half of the row.
 template <int D>
-__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16 *row, bool valid) {
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16 *row, bool valid, int w) {
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
+        if ((c & 1) != w) continue;
         uint32_t v[32];
         if (valid) {
             const uint4 *src = reinterpret_cast<const uint4 *>(row + 64 * c);
@@ -147,24 +160,31 @@ struct DqLayout {
     static constexpr int kTile = 128 * D * 2;
     static constexpr int k_off = 0;
     static constexpr int v_off = k_off + kKStages * kTile;
-    static constexpr int bar_off = v_off + kVStages * kTile;
-    static constexpr int n_bars = 1 + 2 * kKStages + 2 * kVStages + 5;
+    static constexpr int do_off = v_off + kVStages * kTile;   // the CTA's dO tile (read by every dP)
+    static constexpr int bar_off = do_off + kTile;
+    static constexpr int n_bars = 2 + 2 * kKStages + 2 * kVStages + 7;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16 + 1024;
 };
 
-// One CTA = one 128-lane query tile (t) of one query block x one KV head.  The tile's Q and
-// dO rows stay in TMEM for the CTA's lifetime, so S = Q K^T and dP = dO V^T read only the
-// key tile from shared memory.  Per key-tile entry j, with full-width (N = 128) MMAs:
-//   MMA:  S_j = Q K_j^T, dP_j = dO V_j^T                        (into TMEM)
+// One CTA = one 128-lane query tile (t) of one query block x one KV head.  The tile's Q rows
+// stay in TMEM and its dO tile in shared memory for the CTA's lifetime.  Per key-tile entry
+// j, with full-width (N = 128) MMAs:
+//   MMA:  S_j = Q K_j^T (TS), dP_j = dO V_j^T (SS)                        (into TMEM)
 //   EW :  read S_j (frees it: S_{j+1} starts), P_j = exp2(S_j scale log2e - lse) masked
-//   EW :  dS_j = P_j (dP_j - delta), bf16 into the dP columns                  -> ds_full
-//   MMA:  dQ += dS_j K_j, then dP_{j+1}
-// The two elementwise groups split each entry's 128 key columns (64 each); P stays in their
-// registers between the phases.  The chain that sets the pace is dQ_j -> dP_{j+1} -> dS_{j+1};
-// S_{j+1} runs on the tensor core while the groups compute dS_j.
+//   EW :  read dP_j (frees it: dP_{j+1} starts), dS_j = P_j (dP_j - delta) as bf16 into
+//         the dS columns, once dQ_{j-1} has read them                       -> ds_full
+//   MMA:  dQ += dS_j K_j
+// dS has TMEM columns of its own, so no MMA of entry j + 1 waits for dQ_j: while the
+// elementwise groups work on entry j the tensor core runs S_{j+1}, dP_{j+1} and dQ_{j-1}.
+// Two threads issue the MMAs -- warp 9: S and dQ, warp 10: dP -- because issuing a batch
+// blocks the thread while the tensor core's queue is full, and a single issuer then reacts
+// to the elementwise groups' signals late (one issuer: 27.3 ms on the mount-heavy workload,
+// two: 21.6 ms; three, or S+dP / dQ, or S / dP+dQ: 22.7 to 23.5 ms).
+// The two groups split each entry's 128 key columns (64 each); P stays in their registers
+// between the phases.
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
     using L = DqLayout<D>;
@@ -179,28 +199,31 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const int e0 = __ldg(p.blocks + 4 * qb + 2), E = __ldg(p.blocks + 4 * qb + 3) - e0;
     const int4 *entries = reinterpret_cast<const int4 *>(p.entries) + e0;
 
-    const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off;
+    const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off, sDO = sbase + L::do_off;
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
-    const uint32_t qd_ready = bar(0);
-    auto k_full = [&](int s) { return bar(1 + s); };
-    auto k_empty = [&](int s) { return bar(1 + kKStages + s); };
-    auto v_full = [&](int s) { return bar(1 + 2 * kKStages + s); };
-    auto v_empty = [&](int s) { return bar(1 + 2 * kKStages + kVStages + s); };
-    constexpr int kb = 1 + 2 * kKStages + 2 * kVStages;
-    const uint32_t s_full = bar(kb), s_free = bar(kb + 1), dp_full = bar(kb + 2), ds_full = bar(kb + 3);
-    const uint32_t o_full = bar(kb + 4);
+    const uint32_t q_ready = bar(0), do_full = bar(1);
+    auto k_full = [&](int s) { return bar(2 + s); };
+    auto k_empty = [&](int s) { return bar(2 + kKStages + s); };
+    auto v_full = [&](int s) { return bar(2 + 2 * kKStages + s); };
+    auto v_empty = [&](int s) { return bar(2 + 2 * kKStages + kVStages + s); };
+    constexpr int kb = 2 + 2 * kKStages + 2 * kVStages;
+    const uint32_t s_full = bar(kb), s_free = bar(kb + 1), dp_full = bar(kb + 2), dp_free = bar(kb + 3);
+    const uint32_t ds_full = bar(kb + 4), ds_free = bar(kb + 5), o_full = bar(kb + 6);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(qd_ready, 256);
+        mbar_init(q_ready, 256);
+        mbar_init(do_full, 1);
         for (int s = 0; s < kKStages; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
         mbar_init(s_full, 1);
         mbar_init(s_free, 256);
         mbar_init(dp_full, 1);
+        mbar_init(dp_free, 256);
         mbar_init(ds_full, 256);
-        mbar_init(o_full, 1);
+        mbar_init(ds_free, 1);
+        mbar_init(o_full, 2);                 // one commit from each MMA issuer
         *abort = 0;
         fence_barrier_init();
     }
@@ -212,14 +235,22 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns: Q [0, D/2) and dO [64, 64 + D/2) as bf16 pairs, dQ [128, 128 + D),
-    // S [256, 384), dP [384, 512); group w's dS goes to dP columns [384 + 64w, 384 + 64w + 32),
-    // inside the half it has already read.
-    constexpr uint32_t cQ = 0, cDO = 64, cDQ = 128, cS = 256, cDP = 384;
+    // TMEM columns: Q [0, D/2) as bf16 pairs, dS [64, 128) as bf16 pairs (key k in column
+    // 64 + k/2, so group w writes [64 + 32w, 96 + 32w)), dQ [128, 128 + D), S [256, 384),
+    // dP [384, 512).
+    constexpr uint32_t cQ = 0, cDS = 64, cDQ = 128, cS = 256, cDP = 384;
 
     if (warp == 8) {
         const int ppt = kTileRows / p.page_size;
-        if (lane == 0) { tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); }
+        bool do_issued = false;
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_do);
+            if (E > 0) {
+                mbar_arrive_expect_tx(do_full, L::kTile);
+                load_q_tile(sDO, &tm_do, t, g, p.G, p.R, D, q_row0, do_full);
+                do_issued = true;
+            }
+        }
         EntryFeed f;
         int k_issued = 0, v_issued = 0;
         for (int j = 0; j < E; ++j) {
@@ -245,27 +276,26 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
             v_issued = j + 1;
         }
         if (lane == 0) {
+            // wait for this warp's copies still in flight before the CTA can exit
+            if (do_issued) mbar_wait(do_full, 0, nullptr, p.status);
             for (int d = (k_issued > kKStages ? k_issued - kKStages : 0); d < k_issued; ++d)
                 mbar_wait(k_full(d % kKStages), (d / kKStages) & 1, nullptr, p.status);
             for (int d = (v_issued > kVStages ? v_issued - kVStages : 0); d < v_issued; ++d)
                 mbar_wait(v_full(d % kVStages), (d / kVStages) & 1, nullptr, p.status);
         }
     } else if (warp == 9) {
+        // ---------------------------------------------------------------- MMA: S and dQ
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            bool ok = E > 0 && mbar_wait(qd_ready, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status) &&
-                      mbar_wait(v_full(0), 0, abort, p.status);
+            bool ok = E > 0 && mbar_wait(q_ready, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
                 issue_tk<D>(tmem + cS, tmem + cQ, sK, idesc_s);        // S_0 = Q K_0^T
                 mma_commit(s_full);
-                issue_tk<D>(tmem + cDP, tmem + cDO, sV, idesc_s);      // dP_0 = dO V_0^T
-                mma_commit(dp_full);
-                mma_commit(v_empty(0));
             }
             for (int j = 0; ok && j < E; ++j) {
-                const int ks = j % kKStages, ks1 = (j + 1) % kKStages, vs1 = (j + 1) % kVStages;
+                const int ks = j % kKStages, ks1 = (j + 1) % kKStages;
                 if (j + 1 < E) {
                     // S_{j+1} as soon as both groups have read S_j
                     if (!(ok = mbar_wait(s_free, j & 1, abort, p.status) &&
@@ -277,15 +307,34 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 }
                 if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc_split(tmem + cDQ, tmem + cDP, sK + ks * L::kTile, idesc_o, j > 0);   // dQ += dS_j K_j
+                issue_acc(tmem + cDQ, tmem + cDS, sK + ks * L::kTile, idesc_o, j > 0);   // dQ += dS_j K_j
                 mma_commit(k_empty(ks));
-                if (j + 1 < E) {
-                    if (!(ok = mbar_wait(v_full(vs1), ((j + 1) / kVStages) & 1, abort, p.status))) break;
-                    tc_fence_after();
-                    issue_tk<D>(tmem + cDP, tmem + cDO, sV + vs1 * L::kTile, idesc_s);
-                    mma_commit(dp_full);
-                    mma_commit(v_empty(vs1));
-                }
+                mma_commit(ds_free);
+            }
+            mma_commit(o_full);
+            mbar_wait(o_full, 0, nullptr, p.status);
+        }
+    } else if (warp == 10) {
+        // ---------------------------------------------------------------- MMA: dP
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+            bool ok = E > 0 && mbar_wait(do_full, 0, abort, p.status) && mbar_wait(v_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_qk<D>(tmem + cDP, sDO, sV, idesc_s);             // dP_0 = dO V_0^T
+                mma_commit(dp_full);
+                mma_commit(v_empty(0));
+            }
+            for (int j = 0; ok && j + 1 < E; ++j) {
+                // dP_{j+1} as soon as both groups have read dP_j
+                const int vs1 = (j + 1) % kVStages;
+                if (!(ok = mbar_wait(dp_free, j & 1, abort, p.status) &&
+                           mbar_wait(v_full(vs1), ((j + 1) / kVStages) & 1, abort, p.status)))
+                    break;
+                tc_fence_after();
+                issue_qk<D>(tmem + cDP, sDO, sV + vs1 * L::kTile, idesc_s);
+                mma_commit(dp_full);
+                mma_commit(v_empty(vs1));
             }
             mma_commit(o_full);
             mbar_wait(o_full, 0, nullptr, p.status);
@@ -298,12 +347,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const int r_abs = q_row0 + rl, h = g * p.G + hl;
         const bool valid = rl < n_rows;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-        // group 0 puts this lane's Q row into TMEM, group 1 its dO row
-        row_to_tmem<D>(tmem + lane_off + (w == 0 ? cQ : cDO),
-                       (w == 0 ? p.q : p.d_o) + (static_cast<size_t>(r_abs) * p.Hq + h) * D, valid);
+        // the two groups put this lane's Q row into TMEM, half each
+        row_to_tmem<D>(tmem + lane_off + cQ, p.q + (static_cast<size_t>(r_abs) * p.Hq + h) * D, valid, w);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(qd_ready);
+        mbar_arrive(q_ready);
         const float sl2 = p.scale_log2;
         const float *tab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
         const float nlse2 = tab[32 * q4 + lane];      // -lse * log2(e)
@@ -350,6 +398,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_ld32(tmem + lane_off + cDP + 64 * w, dpv[0]);
                 tmem_ld32(tmem + lane_off + cDP + 64 * w + 32, dpv[1]);
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(dp_free);
                 uint32_t ds[2][16];
                 const uint64_t nd2 = f2_pack(ndelta, ndelta);
 #pragma unroll
@@ -360,8 +410,14 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                                             nd2)), r0, r1);
                     ds[i >> 4][i & 15] = pack_bf16(r0, r1);
                 }
-                tmem_st16(tmem + lane_off + cDP + 64 * w, ds[0]);
-                tmem_st16(tmem + lane_off + cDP + 64 * w + 16, ds[1]);
+                // dQ_{j-1} must have read the dS columns before they are overwritten
+                if (j > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (j - 1) & 1, abort, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                tmem_st16(tmem + lane_off + cDS + 32 * w, ds[0]);
+                tmem_st16(tmem + lane_off + cDS + 32 * w + 16, ds[1]);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(ds_full);
@@ -773,7 +829,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
     e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::bytes);
     if (e != cudaSuccess) return e;
     trace_record(trace, 3, stream);
-    dq_kernel<D><<<n_blocks * p.Hkv * 2, kBwdThreads, DqLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    dq_kernel<D><<<n_blocks * p.Hkv * 2, kDqThreads, DqLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::bytes);
     if (e != cudaSuccess) return e;
