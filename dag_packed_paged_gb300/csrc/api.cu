@@ -66,6 +66,29 @@ bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Rank-4 view {64 elements, rows, heads, 64-element chunks} of a bf16 [N, H, D] tensor whose
+// box is one 128-lane query tile of the backward: QB rows x 128 / QB consecutive heads x all
+// D / 64 chunks (QB = min(rows per block, 128)), 128-byte swizzle, zero fill past row N.
+int make_qtile_map(CUtensorMap *m, const void *base, uint64_t N, uint32_t H, uint32_t D, uint32_t qb) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return TA_ERR_CUDA;
+    }
+    cuuint64_t dims[4] = {64, N, H, D / 64};
+    cuuint64_t strides[3] = {uint64_t(H) * D * 2, uint64_t(D) * 2, 128};
+    cuuint32_t box[4] = {64, qb, 128 / qb, D / 64};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (query tile) failed with code " + std::to_string(int(r)));
+        return TA_ERR_CUDA;
+    }
+    return TA_OK;
+}
+
 // Tensor maps for Q-like [N, H, D] and the K/V pools.
 int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
               CUtensorMap *tm_q, CUtensorMap *tm_k, CUtensorMap *tm_v) {
@@ -417,8 +440,10 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &tm_k, &tm_v);
     if (rc) return rc;
     const ta_config &c = h.cfg;
-    if ((rc = make_map(&tm_do, d_o, uint64_t(c.num_q_heads) * c.head_dim, uint64_t(h.N),
-                       uint64_t(c.num_q_heads) * c.head_dim * 2, 64, std::min(h.block_rows, 128))))
+    // the backward loads Q and dO a whole 128-lane tile per box
+    const uint32_t qb = uint32_t(std::min(h.block_rows, 128));
+    if ((rc = make_qtile_map(&tm_q, q, uint64_t(h.N), uint32_t(c.num_q_heads), uint32_t(c.head_dim), qb)) ||
+        (rc = make_qtile_map(&tm_do, d_o, uint64_t(h.N), uint32_t(c.num_q_heads), uint32_t(c.head_dim), qb)))
         return rc;
     BwdParams p{};
     p.blocks = plan->d_blocks;

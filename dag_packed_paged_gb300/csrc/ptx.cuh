@@ -95,6 +95,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// 4D tiled load of one box into shared memory; completion is signalled on `bar` as
+// transaction bytes.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
 // Untiled bulk copy global -> shared (addresses 16-byte aligned, size a multiple of 16),
 // completion signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
