@@ -457,48 +457,84 @@ def main():
     fwd_tflops = flops_fwd / kern_ms["fwd"] / 1e9
 
     # ---------------------------------------------------------------- end to end, host buffers
+    # Every step plans its episode on the host, copies its inputs from pinned host memory and
+    # reads every output back.  Steps are pipelined the way a training loop feeds a GPU: two
+    # sets of device buffers alternate, the copies run on their own streams, and plans are
+    # built and freed in stream order (TA_PLAN_STREAM_ORDERED), so step i's planning and
+    # copies overlap the attention of steps i-1 and i+1.  The timed region starts before the
+    # first step's planning and ends after the last step's outputs are on the host.
     e2e = None
     if not args.no_e2e:
-        h_q = torch.from_numpy(t.q.view(np.int16)).pin_memory()
-        h_k = torch.from_numpy(pool.k_pool.view(np.int16)).pin_memory()
-        h_v = torch.from_numpy(pool.v_pool.view(np.int16)).pin_memory()
-        h_do = torch.from_numpy(t.do.view(np.int16)).pin_memory()
-        outs = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()),
-                (lse, torch.empty(lse.shape, dtype=lse.dtype).pin_memory()),
-                (dq, torch.empty(dq.shape, dtype=dq.dtype).pin_memory()),
-                (dk_pool, torch.empty(dk_pool.shape, dtype=dk_pool.dtype).pin_memory()),
-                (dv_pool, torch.empty(dv_pool.shape, dtype=dv_pool.dtype).pin_memory())]
-        ins = [(q, h_q), (k_pool, h_k), (v_pool, h_v), (d_o, h_do)]
-        h2d = sum(h.numel() * h.element_size() for _, h in ins)
-        d2h = sum(h.numel() * h.element_size() for _, h in outs)
-        e2e_steps = max(2, min(K, 5))
+        h_in = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in (t.q, pool.k_pool, pool.v_pool, t.do)]
+        d_in = [[q, k_pool, v_pool, d_o], [torch.empty_like(x) for x in (q, k_pool, v_pool, d_o)]]
+        d_out = [[o, lse, dq, dk_pool, dv_pool], [torch.empty_like(x) for x in (o, lse, dq, dk_pool, dv_pool)]]
+        h_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in d_out[0]] for _ in range(2)]
+        h2d = sum(h.numel() * h.element_size() for h in h_in)
+        d2h = sum(h.numel() * h.element_size() for h in h_out[0])
+        comp_s, h2d_s, d2h_s = (torch.cuda.Stream(dev) for _ in range(3))
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_read = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):                      # mark both buffer sets free
+            comp_done[b].record(comp_s)
+            out_read[b].record(d2h_s)
+        e2e_steps = max(3, min(K, 6))
 
-        def e2e_step():
-            p2 = plan_now()                                   # host planner + plan upload
-            for dv_, hv in ins:
-                dv_.view(torch.int16).copy_(hv, non_blocking=True)
-            ta.tree_attn_fwd(p2, q, k_pool, v_pool, o, lse)
-            ta.tree_attn_bwd(p2, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, ws)
-            for dv_, hv in outs:
-                hv.copy_(dv_, non_blocking=True)
+        def plan_async():
+            return ta.tree_attn_plan(ep.branches, ep.mounts, pool.page_table, num_q_heads=Hq,
+                                     num_kv_heads=ep.num_kv_heads, head_dim=D, page_size=ep.page_size,
+                                     num_pages=pool.k_pool.shape[0], flags=ta.TA_PLAN_STREAM_ORDERED,
+                                     stream=comp_s)
+
+        def e2e_step(i):
+            b = i % 2
+            p2 = plan_async()                                 # host planner; upload ordered on comp_s
+            h2d_s.wait_event(comp_done[b])                    # step i-2 has finished reading set b
+            with torch.cuda.stream(h2d_s):
+                for dv_, hv in zip(d_in[b], h_in):
+                    dv_.view(torch.int16).copy_(hv, non_blocking=True)
+            in_ready[b].record(h2d_s)
+            comp_s.wait_event(in_ready[b])
+            comp_s.wait_event(out_read[b])                    # step i-2's outputs are on the host
+            qq, kk, vv, dd = d_in[b]
+            oo, ll, gq, gk, gv = d_out[b]
+            ta.tree_attn_fwd(p2, qq, kk, vv, oo, ll, stream=comp_s)
+            ta.tree_attn_bwd(p2, qq, kk, vv, oo, ll, dd, gq, gk, gv, ws, stream=comp_s)
+            comp_done[b].record(comp_s)
+            d2h_s.wait_event(comp_done[b])
+            with torch.cuda.stream(d2h_s):
+                for dv_, hv in zip(d_out[b], h_out[b]):
+                    hv.copy_(dv_, non_blocking=True)
+            out_read[b].record(d2h_s)
             return p2
 
-        keep = e2e_step()
+        for i in range(2):                                    # untimed: one use of each buffer set
+            keep = e2e_step(i)
         torch.cuda.synchronize(dev)
+        ta.tree_attn_check(keep, comp_s)
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            keep = e2e_step()
-        e1.record(stream)
+        e0.record(comp_s)
+        h2d_s.wait_event(e0)
+        d2h_s.wait_event(e0)
+        plans = []
+        for i in range(e2e_steps):
+            plans.append(e2e_step(i))
+            if len(plans) > 2:
+                plans.pop(0)                                  # freed in comp_s order, after its use
+        comp_s.wait_stream(d2h_s)
+        comp_s.wait_stream(h2d_s)
+        e1.record(comp_s)
         torch.cuda.synchronize(dev)
-        del keep
+        ta.tree_attn_check(plans[-1], comp_s)
+        del keep, plans
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
         e2e = {"value": (flops_fwd + flops_bwd) * world / e2e_ms / 1e9, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-               "steps": e2e_steps, "includes": "plan + H2D of q/k_pool/v_pool/dO from pinned host + fwd + bwd "
-                                               "+ D2H of o/lse/dq/dk_pool/dv_pool"}
+               "steps": e2e_steps, "includes": "per step: plan + H2D of q/k_pool/v_pool/dO from pinned host + fwd "
+                                               "+ bwd + D2H of o/lse/dq/dk_pool/dv_pool; steps pipelined over two "
+                                               "buffer sets and three streams"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,

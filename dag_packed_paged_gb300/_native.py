@@ -27,6 +27,7 @@ TA_CLAMP_MOUNTS = 0x1
 TA_NO_MOUNTS = 0x2
 TA_TRANSITIVE_MOUNTS = 0x4
 TA_PLAN_HOST_ONLY = 0x100
+TA_PLAN_STREAM_ORDERED = 0x200
 
 HEADER = os.path.join(INCLUDE, "treeattn.h")
 

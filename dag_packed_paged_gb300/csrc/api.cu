@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -104,6 +105,65 @@ int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void
     return make_map(tm_v, v_pool, inner, pool_rows, inner * 2, 64, c.page_size);
 }
 
+// Stream-ordered plan upload (TA_PLAN_STREAM_ORDERED).  A copy from pageable memory is staged
+// by the driver in chunks whose DMA is queued on the copy's stream, so on a stream still busy
+// with earlier kernels the call blocks the host until they finish.  The upload therefore runs
+// on an internal stream that nothing else uses, from a pinned staging buffer reused across
+// plans, and the caller's stream waits for it through an event: the host never waits for the
+// caller's earlier work.
+struct Uploader {
+    std::mutex mu;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t done = nullptr;   // recorded after the last copy out of `pinned`
+    void *pinned = nullptr;
+    size_t cap = 0;
+};
+constexpr int kMaxUploadDevices = 64;
+Uploader g_uploader[kMaxUploadDevices];
+
+// Allocates *dst (stream-ordered) and copies `bytes` from host `src` into it; work enqueued on
+// `user` after this call is ordered after the copy.
+int upload_stream_ordered(int dev, void **dst, const void *src, size_t bytes, cudaStream_t user) {
+    if (dev < 0 || dev >= kMaxUploadDevices) {
+        set_error("device index beyond the supported range");
+        return TA_ERR_UNSUPPORTED;
+    }
+    Uploader &u = g_uploader[dev];
+    std::lock_guard<std::mutex> lock(u.mu);
+    cudaError_t e = cudaSuccess;
+    if (!u.stream) e = cudaStreamCreateWithFlags(&u.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess && !u.done) e = cudaEventCreateWithFlags(&u.done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventSynchronize(u.done);   // the previous copy has left `pinned`
+    if (e == cudaSuccess && u.cap < bytes) {
+        if (u.pinned) cudaFreeHost(u.pinned);
+        u.pinned = nullptr;
+        u.cap = 0;
+        e = cudaMallocHost(&u.pinned, bytes);
+        if (e == cudaSuccess) u.cap = bytes;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload (staging)");
+    std::memcpy(u.pinned, src, bytes);
+    *dst = nullptr;
+    e = cudaMallocAsync(dst, bytes, u.stream);
+    if (e != cudaSuccess) {
+        *dst = nullptr;
+        if (e == cudaErrorMemoryAllocation) {
+            set_error("device allocation failed");
+            return TA_ERR_NOMEM;
+        }
+        return cuda_fail(e, "plan upload (allocation)");
+    }
+    e = cudaMemcpyAsync(*dst, u.pinned, bytes, cudaMemcpyHostToDevice, u.stream);
+    if (e == cudaSuccess) e = cudaEventRecord(u.done, u.stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, u.done, 0);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(*dst, u.stream);
+        *dst = nullptr;
+        return cuda_fail(e, "plan upload");
+    }
+    return TA_OK;
+}
+
 }  // namespace
 }  // namespace treeattn
 
@@ -173,21 +233,34 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     std::vector<uint8_t> staging(total, 0);
     for (Part &p : parts)
         if (p.src && p.bytes) std::memcpy(staging.data() + p.off, p.src, p.bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    plan->stream_ordered = (h.cfg.flags & TA_PLAN_STREAM_ORDERED) != 0;
+    plan->stream = stream;
     cudaError_t e = cudaGetDevice(&plan->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device);
-    if (e == cudaSuccess) e = cudaMalloc(&plan->d_buf, total);
     if (e != cudaSuccess) {
-        delete plan;
-        return e == cudaErrorMemoryAllocation ? (set_error("device allocation failed"), TA_ERR_NOMEM)
-                                              : cuda_fail(e, "plan upload");
-    }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = cudaMemcpyAsync(plan->d_buf, staging.data(), total, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) {
-        cudaFree(plan->d_buf);
         delete plan;
         return cuda_fail(e, "plan upload");
+    }
+    if (plan->stream_ordered) {
+        if ((rc = upload_stream_ordered(plan->device, &plan->d_buf, staging.data(), total, s))) {
+            delete plan;
+            return rc;
+        }
+    } else {
+        e = cudaMalloc(&plan->d_buf, total);
+        if (e != cudaSuccess) {
+            delete plan;
+            return e == cudaErrorMemoryAllocation ? (set_error("device allocation failed"), TA_ERR_NOMEM)
+                                                  : cuda_fail(e, "plan upload");
+        }
+        e = cudaMemcpyAsync(plan->d_buf, staging.data(), total, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) {
+            cudaFree(plan->d_buf);
+            delete plan;
+            return cuda_fail(e, "plan upload");
+        }
     }
     uint8_t *d = static_cast<uint8_t *>(plan->d_buf);
     plan->d_buf = d;
@@ -209,7 +282,10 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
 
 void tree_attn_plan_destroy(ta_plan *plan) {
     if (!plan) return;
-    if (plan->d_buf) cudaFree(plan->d_buf);
+    if (plan->d_buf) {
+        if (plan->stream_ordered) cudaFreeAsync(plan->d_buf, static_cast<cudaStream_t>(plan->stream));
+        else cudaFree(plan->d_buf);
+    }
     delete plan;
 }
 

@@ -72,5 +72,7 @@ struct ta_plan {
     size_t ws_bytes = 0;              // total bwd workspace
     int device = 0;
     int num_sms = 0;
+    bool stream_ordered = false;      // TA_PLAN_STREAM_ORDERED: d_buf is freed with cudaFreeAsync on `stream`
+    void *stream = nullptr;           // cudaStream_t given to tree_attn_plan
     void *trace[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};  // cudaEvent_t
 };

@@ -58,6 +58,19 @@ extern "C" {
 #define TA_PLAN_HOST_ONLY 0x100u /* build the plan on the host only (no device upload, no GPU
                                     needed): for inspection with tree_attn_plan_export/_stats;
                                     tree_attn_fwd/_bwd reject such a plan */
+#define TA_PLAN_STREAM_ORDERED 0x200u /* build and destroy the plan without waiting for the
+                                    GPU: the device arrays are allocated (cudaMallocAsync) and
+                                    uploaded from a pinned staging buffer on an internal stream
+                                    of the library, `stream` is made to wait for that upload
+                                    (an event), and tree_attn_plan_destroy frees them with
+                                    cudaFreeAsync on `stream`.  Without the flag tree_attn_plan
+                                    synchronises `stream` before returning and destroy uses
+                                    cudaFree, which waits for the whole device.  With it the
+                                    plan may be used on `stream` right away, or on another
+                                    stream after an event recorded on `stream` after the plan
+                                    call; every use on other streams must be ordered before
+                                    work enqueued on `stream` after destroy, and `stream` must
+                                    still exist then. */
 
 /* A branch: `length` rows stored at compact rows [row_start, row_start + length).
  * parent = -1 for a root (fork_offset must be 0); otherwise the child shares the parent's
@@ -194,7 +207,7 @@ int tree_attn_owner_mask(const int64_t *offsets, int32_t n_traj, const int64_t *
  * per block the visible key-row intervals (Eq. 4 gather, expressed as row intervals rather
  * than copied), translates them into 128-row key tiles, builds the key-tile-major transpose
  * used by the dK/dV reduction, and uploads everything to the device on `stream`
- * (synchronising once).
+ * (synchronising once, or not at all with TA_PLAN_STREAM_ORDERED).
  *
  *   branches[n_branches], mounts[n_mounts]   host arrays, read during the call only
  *   page_table[n_logical_pages]             host: logical page l of the strip (rows
