@@ -303,3 +303,19 @@ def test_no_mounts_plan_equals_mount_free_plan_except_positions():
     for key in ("blocks", "blk_iv_ptr", "iv_lo", "iv_hi", "diag", "entries", "t_entries", "chunks"):
         assert np.array_equal(a[key], b[key]), key
     assert np.array_equal(a["pos_ids"], dag.positions(ep.branches, ep.mounts))
+
+
+def test_stream_ordered_flag_leaves_the_plan_unchanged():
+    """TA_PLAN_STREAM_ORDERED changes only how the device copy is made: the host plan (every
+    exported array and the stats) is the same as without it."""
+    ep = W.scaled(2, 32)
+    a = host_plan(ep)
+    b = host_plan(ep, flags=ta.TA_PLAN_STREAM_ORDERED)
+    ea, eb = ta.tree_attn_plan_export(a), ta.tree_attn_plan_export(b)
+    assert ea.keys() == eb.keys()
+    for k in ea:
+        assert np.array_equal(np.asarray(ea[k]), np.asarray(eb[k])), k
+    sa, sb = ta.tree_attn_plan_stats(a), ta.tree_attn_plan_stats(b)
+    for k in sa:
+        if k != "plan_ms":
+            assert sa[k] == sb[k], k
