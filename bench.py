@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -87,9 +88,9 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, dev_uuid=None):
+    def __init__(self, dev_uuid=None, path=None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"treeattn_clocks_{os.getpid()}.csv")
         self.uuid = dev_uuid
 
     def __enter__(self):
@@ -345,6 +346,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clock-log", default=None, help="keep the raw nvidia-smi clock samples in this CSV file")
     ap.add_argument("--op", default="attention", choices=["attention", "rope", "logprob"],
                     help="attention: the forward + backward step (the headline); rope: the RoPE kernel alone; "
                          "logprob: compact log-probabilities forward + backward (vocabulary 151,936)")
@@ -424,7 +426,7 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(uuid if rank == 0 else None) as clocks:
+    with ClockSampler(uuid if rank == 0 else None, args.clock_log) as clocks:
         time.sleep(0.3)
         ev0.record(stream)
         for k in range(K):

@@ -271,7 +271,7 @@ def mount_heavy(seed: int = 0, n_dags: int = 4) -> Episode:
                    16, 4, 128, 64, seed)
 
 
-CONFIGS = {
+_WORKLOAD_MAKERS = {
     0: tiny,
     1: balanced,
     2: commander_worker,
@@ -281,13 +281,13 @@ CONFIGS = {
 
 
 def config(i: int) -> Episode:
-    return CONFIGS[i]()
+    return _WORKLOAD_MAKERS[i]()
 
 
 def scaled(i: int, factor: int, seed: int = 0) -> Episode:
     """The shape of workload ``i`` with every length divided by ``factor`` (rounded, at least
     a few rows), keeping heads/D/page: a parity case the oracle finishes in seconds."""
-    ep = CONFIGS[i]()
+    ep = _WORKLOAD_MAKERS[i]()
     br = ep.branches.copy()
     sc = lambda x: max(3, int(round(x / factor)))
     new_len = [sc(int(l)) for l in br["length"]]

@@ -35,7 +35,7 @@ extern "C" {
 
 #define TA_OK 0
 #define TA_ERR_INVALID (-1)         /* malformed DAG, page table or arguments */
-#define TA_ERR_UNSUPPORTED (-2)     /* a shape this build does not implement */
+#define TA_ERR_UNSUPPORTED (-2)     /* a shape the library does not implement */
 #define TA_ERR_NOMEM (-3)           /* host or device allocation failed (planner only) */
 #define TA_ERR_CUDA (-4)            /* a CUDA runtime/driver call failed */
 #define TA_ERR_DEVICE_TIMEOUT (-5)  /* a bounded device-side wait expired; outputs are invalid */
