@@ -294,9 +294,10 @@ int tree_attn_logprob_index(const int64_t *pos_row, const int32_t *pos_target, i
  *   o       device bf16 [N, Hq, D] (written)
  *   lse     device fp32 [Hq, N] (written), natural log
  * Everything is enqueued on `stream`; no allocation, no synchronisation.  Caller owns every
- * buffer.  Returns TA_ERR_INVALID for NULL/misaligned pointers, TA_ERR_CUDA for a launch
- * failure, TA_ERR_DEVICE_TIMEOUT if an earlier launch on this plan reported an expired
- * bounded wait (the status is read back only by tree_attn_check).
+ * buffer.  Returns TA_ERR_INVALID for NULL/misaligned pointers or a host-only plan, and
+ * TA_ERR_CUDA for a launch failure.  A bounded device-side wait that expires inside the
+ * launched kernels is not seen by this call: it is recorded in the plan's status words and
+ * reported by the next tree_attn_check on the plan (TA_ERR_DEVICE_TIMEOUT).
  */
 int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
                   void *o, float *lse, void *stream);
@@ -333,10 +334,9 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
  * no counterpart to this; it exists for callers that cannot give the library device scratch:
  * plugin-style hosts that pass a kernel only its input and output buffers, and loops that
  * forbid device allocation while running (cudaMalloc can synchronise the device and may fail
- * or fragment a sized pool).  It allocates nothing.  The scratch (the lse/delta table and dK/dV
- * partials)
- * is a fixed 64 MiB array inside the library that every GPU loading the library holds until
- * the process exits; plans needing more (tree_attn_bwd_workspace_size(plan) > 64 MiB) are
+ * or fragment a sized pool).  It allocates nothing.  The scratch (the lse/delta table and the
+ * dK/dV partials) is a fixed 64 MiB array inside the library that every GPU loading the
+ * library holds until the process exits; plans needing more (tree_attn_bwd_workspace_size(plan) > 64 MiB) are
  * rejected with TA_ERR_UNSUPPORTED and a message naming the size.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device current; make
  * that first call before any stream capture.  All calls share the array and nothing in it
