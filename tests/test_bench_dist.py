@@ -59,3 +59,26 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
 
     bench.run_reference(A(), W.tiny(), world=2, rank=1)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_has_the_contract_keys(capsys):
+    import json
+
+    import bench
+    from dag_packed_paged_gb300 import workloads as W
+
+    class A:
+        steps, warmup, workload = 1, 0, "tiny_tree"
+
+    bench.run_reference(A(), W.tiny(), world=1, rank=0)
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1
+    line = json.loads(out[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "TFLOP/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"] and line["e2e"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["name"] == "tiny_tree"
