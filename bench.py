@@ -174,11 +174,15 @@ def cpu_baseline(ep, t, target_s=15.0, seed=0):
         pairs = int((iv[3] - iv[2]).sum())
         return dt, pairs, b.threads
 
-    probe = rng.choice(N, 8, replace=False)
-    dt, pairs, _ = run(probe)
-    n = int(min(4096, max(16, 8 * target_s / max(dt, 1e-3))))
-    rows = rng.choice(N, n, replace=False)
-    dt, pairs, threads = run(rows)
+    # size the sample from a probe, then correct once: the probe's fixed costs make a
+    # straight extrapolation undershoot
+    n = 32
+    dt, pairs, _ = run(rng.choice(N, n, replace=False))
+    for _ in range(2):
+        n = int(min(4096, max(16, n * target_s / max(dt, 1e-3))))
+        dt, pairs, threads = run(rng.choice(N, n, replace=False))
+        if dt >= 0.6 * target_s or n >= 4096:
+            break
     flops = 14.0 * ep.head_dim * ep.num_q_heads * pairs
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "seconds": round(dt, 2),
