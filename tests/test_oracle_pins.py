@@ -141,6 +141,8 @@ def test_irregular_search_matches_recorded():
     ep = W.irregular()
     assert 126_000 <= ep.n_rows <= 130_000
     assert len(ep.branches) == 64
+    # the shape statistic the irregular tree copies: about 5.6 expanded rows per compact row
+    assert abs(ep.info["expanded_rows"] / ep.n_rows - 5.6) <= 0.1
 
 
 def test_tiny_pair_count():
