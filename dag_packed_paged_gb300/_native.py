@@ -53,7 +53,8 @@ class ta_config(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("flags", ctypes.c_uint32),
-                ("num_pages", ctypes.c_int64)]
+                ("num_pages", ctypes.c_int64), ("num_sms", ctypes.c_int32),
+                ("dkdv_chunk_entries", ctypes.c_int32)]
 
 
 class ta_plan_stats(ctypes.Structure):
@@ -64,7 +65,8 @@ class ta_plan_stats(ctypes.Structure):
                 ("n_kv_tiles", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
                 ("n_partial_slots", ctypes.c_int64), ("block_rows", ctypes.c_int32),
                 ("tile_rows", ctypes.c_int32), ("bwd_workspace_bytes", ctypes.c_size_t),
-                ("plan_ms", ctypes.c_double)]
+                ("plan_ms", ctypes.c_double), ("chunk_cap", ctypes.c_int64), ("num_sms", ctypes.c_int32),
+                ("device", ctypes.c_int32)]
 
 
 _P32 = ctypes.POINTER(ctypes.c_int32)
@@ -188,14 +190,16 @@ class Plan:
 def tree_attn_plan(branches: np.ndarray, mounts: np.ndarray, page_table: np.ndarray, *,
                    num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                    num_pages: int, softmax_scale: float = 0.0, flags: int = 0,
-                   stream=None) -> Plan:
+                   stream=None, num_sms: int = 0, dkdv_chunk_entries: int = 0) -> Plan:
     """branches: structured array with fields parent, fork_offset, length, row_start (the
-    ta_branch layout); mounts: reader, reader_offset, source, src_begin, src_end."""
+    ta_branch layout); mounts: reader, reader_offset, source, src_begin, src_end.
+    num_sms / dkdv_chunk_entries: the dK/dV work-balance knobs of ta_config (0: defaults)."""
     br = np.ascontiguousarray(branches)
     mt = np.ascontiguousarray(mounts)
     assert br.dtype.itemsize == ctypes.sizeof(ta_branch) and mt.dtype.itemsize == ctypes.sizeof(ta_mount)
     pt = np.ascontiguousarray(page_table, dtype=np.int32)
-    cfg = ta_config(num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale, flags, num_pages)
+    cfg = ta_config(num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale, flags, num_pages,
+                    num_sms, dkdv_chunk_entries)
     n_rows = int((br["row_start"] + br["length"]).max()) if len(br) else 0
     pos = np.zeros(max(n_rows, 1), dtype=np.int32)
     h = ctypes.c_void_p()

@@ -186,10 +186,19 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         set_error("host allocation failed");
         return TA_ERR_NOMEM;
     }
+    int device_sms = 0;
+    if (config && !(config->flags & TA_PLAN_HOST_ONLY)) {
+        cudaError_t e = cudaGetDevice(&plan->device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&device_sms, cudaDevAttrMultiProcessorCount, plan->device);
+        if (e != cudaSuccess) {
+            delete plan;
+            return cuda_fail(e, "tree_attn_plan: device query");
+        }
+    }
     int rc;
     try {
         rc = build_host_plan(branches, n_branches, mounts, n_mounts, page_table, n_logical_pages, config,
-                             plan->host);
+                             device_sms, plan->host);
     } catch (const std::bad_alloc &) {
         set_error("host allocation failed while planning");
         rc = TA_ERR_NOMEM;
@@ -236,12 +245,7 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     plan->stream_ordered = (h.cfg.flags & TA_PLAN_STREAM_ORDERED) != 0;
     plan->stream = stream;
-    cudaError_t e = cudaGetDevice(&plan->device);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device);
-    if (e != cudaSuccess) {
-        delete plan;
-        return cuda_fail(e, "plan upload");
-    }
+    cudaError_t e = cudaSuccess;
     if (plan->stream_ordered) {
         if ((rc = upload_stream_ordered(plan->device, &plan->d_buf, staging.data(), total, s))) {
             delete plan;
@@ -322,6 +326,9 @@ int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out) {
     out->tile_rows = kTileRows;
     out->bwd_workspace_bytes = plan->ws_bytes;
     out->plan_ms = h.plan_ms;
+    out->chunk_cap = h.chunk_cap;
+    out->num_sms = h.num_sms;
+    out->device = plan->device;
     return TA_OK;
 }
 
@@ -355,22 +362,40 @@ static bool host_only(const ta_plan *plan) {
     return true;
 }
 
+// The plan's arrays live on the device it was built on: launching with another device current
+// would read them through the wrong GPU.  TA_OK, or TA_ERR_INVALID / TA_ERR_CUDA with a message.
+static int check_device(const ta_plan *plan, const char *who) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    if (dev != plan->device) {
+        set_error(std::string(who) + ": the plan was built on device " + std::to_string(plan->device) +
+                  " but device " + std::to_string(dev) + " is current");
+        return TA_ERR_INVALID;
+    }
+    return TA_OK;
+}
+
 int tree_attn_check(const ta_plan *plan, void *stream) {
     if (!plan) {
         set_error("plan is NULL");
         return TA_ERR_INVALID;
     }
     if (host_only(plan)) return TA_ERR_INVALID;
+    if (int rc = check_device(plan, "tree_attn_check")) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     int32_t st[4] = {0, 0, 0, 0};
-    e = cudaMemcpy(st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost);
+    e = cudaMemcpyAsync(st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     const int32_t any = st[0] | st[1] | st[2] | st[3];
     if (any) {
-        cudaMemset(plan->d_status, 0, sizeof(st));
-        cudaDeviceSynchronize();
+        // clear on the same stream; only this stream waits for it
+        e = cudaMemsetAsync(plan->d_status, 0, sizeof(st), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "status clear");
         if (any & kStatusTimeout) {
             set_error("a bounded device-side wait expired; outputs of the affected launches are invalid");
             return TA_ERR_DEVICE_TIMEOUT;
@@ -434,6 +459,7 @@ int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base
     }
     if (h.N == 0) return TA_OK;
     if (host_only(plan)) return TA_ERR_INVALID;
+    if (int rc = check_device(plan, "tree_attn_rope")) return rc;
     if (!aligned16(q) || !aligned16(k_pool)) {
         set_error("tree_attn_rope: NULL or misaligned (16-byte) pointer");
         return TA_ERR_INVALID;
@@ -462,6 +488,7 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     const HostPlan &h = plan->host;
     if (h.N == 0) return TA_OK;
     if (host_only(plan)) return TA_ERR_INVALID;
+    if (int rc = check_device(plan, "tree_attn_fwd")) return rc;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(lse)) {
         set_error("tree_attn_fwd: NULL or misaligned (16-byte) pointer");
         return TA_ERR_INVALID;
@@ -503,6 +530,7 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     const HostPlan &h = plan->host;
     if (h.N == 0) return TA_OK;
     if (host_only(plan)) return TA_ERR_INVALID;
+    if (int rc = check_device(plan, "tree_attn_bwd")) return rc;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(lse) ||
         !aligned16(d_o) || !aligned16(dq) || !aligned16(dk_pool) || !aligned16(dv_pool)) {
         set_error("tree_attn_bwd: NULL or misaligned (16-byte) pointer");

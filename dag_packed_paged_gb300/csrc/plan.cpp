@@ -55,7 +55,7 @@ int fail(int code, const std::string &msg) {
 
 int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts,
                     int32_t n_mounts, const int32_t *page_table, int64_t n_logical_pages,
-                    const ta_config *config, HostPlan &P) {
+                    const ta_config *config, int device_sms, HostPlan &P) {
     auto t_start = std::chrono::steady_clock::now();
     if (!config) return fail(TA_ERR_INVALID, "config is NULL");
     if (n_branches < 0 || n_mounts < 0) return fail(TA_ERR_INVALID, "negative count");
@@ -411,9 +411,12 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
             }
     }
     // chunks: bound the entries per dK/dV work item so that no item is much longer than a
-    // fraction of the average per-SM share (the work per entry is about constant)
+    // quarter of the average per-SM share (the work per entry is about constant)
+    P.num_sms = c.num_sms > 0 ? c.num_sms : (device_sms > 0 ? device_sms : kDefaultSms);
     const int64_t work = n_entries * c.num_kv_heads;
-    const int64_t cap = std::max<int64_t>(8, work / (152 * 4));
+    const int64_t cap = c.dkdv_chunk_entries > 0 ? int64_t(c.dkdv_chunk_entries)
+                                                 : std::max<int64_t>(8, work / (int64_t(P.num_sms) * 4));
+    P.chunk_cap = cap;
     std::vector<std::array<int64_t, 4>> ch;
     for (int64_t k = 0; k < n_tiles; ++k) {
         const int64_t a = tptr[k], z = tptr[k + 1];

@@ -41,14 +41,19 @@ struct HostPlan {
     std::vector<int32_t> t_info;      // per tile-major entry: block << 2 | flags, first row, lo, hi
     int64_t n_segments = 0;
     int64_t n_partial_slots = 0;
+    int64_t chunk_cap = 0;            // entries per dK/dV chunk at most
+    int32_t num_sms = 0;              // SM count the cap was derived from
     int64_t pairs = 0;
     double plan_ms = 0.0;
 };
 
-// Builds the host plan; returns TA_OK or an error code (message via set_error).
+constexpr int kDefaultSms = 152;     // GB300; used when neither the config nor a device gives one
+
+// Builds the host plan; returns TA_OK or an error code (message via set_error).  device_sms:
+// the SM count of the device the plan is for (0: none, e.g. a host-only plan).
 int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts,
                     int32_t n_mounts, const int32_t *page_table, int64_t n_logical_pages,
-                    const ta_config *config, HostPlan &out);
+                    const ta_config *config, int device_sms, HostPlan &out);
 
 }  // namespace treeattn
 
@@ -70,8 +75,7 @@ struct ta_plan {
     int32_t *d_status = nullptr;      // bounded-wait status words (zeroed at plan time)
     size_t ws_table_bytes = 0;        // workspace: per (KV head, block, query tile) 128 lse*log2e + 128 delta
     size_t ws_bytes = 0;              // total bwd workspace
-    int device = 0;
-    int num_sms = 0;
+    int device = -1;                  // -1: host-only plan
     bool stream_ordered = false;      // TA_PLAN_STREAM_ORDERED: d_buf is freed with cudaFreeAsync on `stream`
     void *stream = nullptr;           // cudaStream_t given to tree_attn_plan
     void *trace[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};  // cudaEvent_t

@@ -46,6 +46,11 @@ int tree_attn_selftest_timeout(const ta_plan *plan, int64_t limit_us, void *stre
         set_error("the plan was built with TA_PLAN_HOST_ONLY");
         return TA_ERR_INVALID;
     }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) {
+        set_error("tree_attn_selftest_timeout: the plan's device is not the current device");
+        return TA_ERR_INVALID;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     timeout_selftest_kernel<<<1, 32, 0, s>>>(plan->d_status + 3,
                                              static_cast<unsigned long long>(limit_us) * 1000ull);

@@ -98,7 +98,14 @@ typedef struct {
 /* Attention shape.  Supported: head_dim 64 or 128; page_size 16, 32, 64 or 128;
  * num_q_heads / num_kv_heads (query heads per KV head, consecutive grouping: query head h
  * uses KV head h / G) in {1, 2, 4, 8, 16}.  softmax_scale <= 0 selects 1/sqrt(head_dim).
- * num_pages is the number of pages in the K/V pools (>= the logical pages of the strip). */
+ * num_pages is the number of pages in the K/V pools (>= the logical pages of the strip).
+ *
+ * Work balance of the dK/dV kernel (no effect on results beyond fp32 summation order): the
+ * readers of a key tile are split into chunks of at most `dkdv_chunk_entries` (query block,
+ * key tile) entries, each chunk one CTA, whose partial sums a fixed-order reduction adds.
+ * dkdv_chunk_entries <= 0 selects max(8, entries * num_kv_heads / (4 * SMs)): no chunk longer
+ * than about a quarter of an SM's average share.  SMs = num_sms if > 0, else the SM count of
+ * the current device (152 on GB300) -- or 152 for a TA_PLAN_HOST_ONLY plan, which has no device. */
 typedef struct {
     int32_t num_q_heads;
     int32_t num_kv_heads;
@@ -107,6 +114,8 @@ typedef struct {
     float softmax_scale;
     uint32_t flags;
     int64_t num_pages;
+    int32_t num_sms;             /* 0: the device's (see above) */
+    int32_t dkdv_chunk_entries;  /* 0: derived from the SM count (see above) */
 } ta_config;
 
 typedef struct ta_plan ta_plan; /* opaque; owned by the library */
@@ -128,6 +137,9 @@ typedef struct {
     int32_t tile_rows;       /* key rows per tile (128) */
     size_t bwd_workspace_bytes;
     double plan_ms;          /* host time spent in tree_attn_plan */
+    int64_t chunk_cap;       /* entries per dK/dV chunk at most (see ta_config) */
+    int32_t num_sms;         /* SM count the chunk cap was derived from */
+    int32_t device;          /* CUDA device the plan was uploaded to (-1: host-only plan) */
 } ta_plan_stats;
 
 /* Host views of the plan's arrays, for inspection and bit-exact tests.  All pointers are
@@ -294,8 +306,10 @@ int tree_attn_logprob_index(const int64_t *pos_row, const int32_t *pos_target, i
  *   o       device bf16 [N, Hq, D] (written)
  *   lse     device fp32 [Hq, N] (written), natural log
  * Everything is enqueued on `stream`; no allocation, no synchronisation.  Caller owns every
- * buffer.  Returns TA_ERR_INVALID for NULL/misaligned pointers or a host-only plan, and
- * TA_ERR_CUDA for a launch failure.  A bounded device-side wait that expires inside the
+ * buffer.  Returns TA_ERR_INVALID for NULL/misaligned pointers, a host-only plan, or a plan
+ * built while another device was current (the plan's arrays live on that device; the same
+ * check guards tree_attn_bwd, tree_attn_rope and tree_attn_check), and TA_ERR_CUDA for a
+ * launch failure.  A bounded device-side wait that expires inside the
  * launched kernels is not seen by this call: it is recorded in the plan's status words and
  * reported by the next tree_attn_check on the plan (TA_ERR_DEVICE_TIMEOUT).
  */
@@ -337,9 +351,11 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
  * or fragment a sized pool).  It allocates nothing.  The scratch (the lse/delta table and the
  * dK/dV partials) is a fixed 64 MiB array inside the library that every GPU loading the
  * library holds until the process exits; plans needing more (tree_attn_bwd_workspace_size(plan) > 64 MiB) are
- * rejected with TA_ERR_UNSUPPORTED and a message naming the size.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that device current; make
- * that first call before any stream capture.  All calls share the array and nothing in it
+ * rejected with TA_ERR_UNSUPPORTED and a message naming the size.  Every call looks up the
+ * array's device address (cudaGetSymbolAddress) with the current device, which must be the
+ * plan's (TA_ERR_INVALID otherwise), so the address stays right after a context reset; the
+ * first call on a device may load the library's module there, so make that first call before
+ * any stream capture.  All calls share the array and nothing in it
  * needs clearing between calls, so calls whose kernels overlap on the GPU (other streams or
  * host threads) race on it: serialise them.  Arguments, outputs and other errors are those of
  * tree_attn_bwd.
@@ -354,7 +370,7 @@ size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
 
 /* Synchronises `stream` and reports whether any bounded device wait of this plan's kernels
  * expired since the last check (TA_ERR_DEVICE_TIMEOUT) or a CUDA error is pending
- * (TA_ERR_CUDA); clears the status. */
+ * (TA_ERR_CUDA); clears the status with a copy on `stream` (other streams are not waited for). */
 int tree_attn_check(const ta_plan *plan, void *stream);
 
 /* Diagnostic: runs the bounded-wait error path on purpose.  Launches one kernel on `stream`

@@ -138,6 +138,10 @@ def test_crafted():
     check_plan_against_oracle(crafted())
 
 
+def test_wide_fan():
+    check_plan_against_oracle(W.wide_fan())
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_zero_length_mounts_give_identical_plan(seed):
     ep = W.random_small(seed, max_len=200)
@@ -319,3 +323,46 @@ def test_stream_ordered_flag_leaves_the_plan_unchanged():
     for k in sa:
         if k != "plan_ms":
             assert sa[k] == sb[k], k
+
+
+def _chunk_lengths(ex):
+    ch = ex["chunks"]
+    return ch[:, 2] - ch[:, 1]
+
+
+@pytest.mark.parametrize("make", [lambda: W.config(1), lambda: W.scaled(4, 8)], ids=["balanced", "mount_heavy/8"])
+def test_chunk_cap_follows_sm_count(make):
+    """Without an explicit cap, a key tile's readers are split into chunks of at most
+    max(8, entries * Hkv / (4 * SMs)) entries: fewer SMs give longer chunks and fewer of them."""
+    ep = make()
+    counts = {}
+    for sms in (38, 76, 152, 304):
+        plan = host_plan(ep, num_sms=sms)
+        st = ta.tree_attn_plan_stats(plan)
+        ex = ta.tree_attn_plan_export(plan)
+        cap = max(8, st["n_entries"] * ep.num_kv_heads // (4 * sms))
+        assert st["chunk_cap"] == cap and st["num_sms"] == sms
+        assert _chunk_lengths(ex).max() <= cap
+        counts[sms] = st["n_chunks"]
+    assert counts[38] <= counts[76] <= counts[152] <= counts[304]
+    assert counts[38] < counts[304]
+    # a host-only plan has no device: 152 SMs unless the config names a count
+    st = ta.tree_attn_plan_stats(host_plan(ep))
+    assert st["num_sms"] == 152 and st["device"] == -1
+
+
+def test_chunk_cap_override_gives_unsplit_long_chunks():
+    """dkdv_chunk_entries forces the chunk length: a large cap leaves every key tile unsplit
+    (no partial slots); a cap of 1 splits every tile into single entries."""
+    ep = W.wide_fan()
+    big = host_plan(ep, dkdv_chunk_entries=1 << 20)
+    st, ex = ta.tree_attn_plan_stats(big), ta.tree_attn_plan_export(big)
+    assert st["n_partial_slots"] == 0 and st["chunk_cap"] == 1 << 20
+    assert st["n_chunks"] == len(np.unique(ex["t_entries"][:, 1] // T))
+    assert _chunk_lengths(ex).max() >= 200
+    one = host_plan(ep, dkdv_chunk_entries=1)
+    st1, ex1 = ta.tree_attn_plan_stats(one), ta.tree_attn_plan_export(one)
+    assert (_chunk_lengths(ex1) == 1).all() and st1["n_chunks"] == st1["n_entries"]
+    # the chunking changes nothing else in the plan
+    for key in ("blocks", "entries", "t_entries"):
+        assert np.array_equal(ex[key], ex1[key])
