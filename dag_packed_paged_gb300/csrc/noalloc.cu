@@ -11,14 +11,16 @@
 //
 // The array below is a file-scope __device__ variable: every GPU that loads the library
 // holds all of it until the process exits.  In host code its name is only a host-side
-// stand-in, not a device address, so the entry point looks the address up with
-// cudaGetSymbolAddress (once per device, with that device current) and passes that pointer
-// on.  Nothing in it needs clearing: every byte the backward reads from the scratch is
-// written earlier in the same call.  All calls share the array, so calls whose kernels
-// overlap on the GPU (different streams, or different host threads) race on it.
+// stand-in, not a device address, so every call looks the address up with
+// cudaGetSymbolAddress, with the plan's device current, and passes that pointer on.  Looking it
+// up on each call (a cheap runtime query) keeps the address right after the device's context
+// is reset and re-created.  The first call on a device may load the library's module there;
+// make that first call before any stream capture.  Nothing in the array needs clearing: every
+// byte the backward reads from the scratch is written earlier in the same call.  All calls
+// share the array, so calls whose kernels overlap on the GPU (different streams, or different
+// host threads) race on it.
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <string>
 
 #include "../../include/treeattn.h"
@@ -32,33 +34,26 @@ constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_bwd_scratch on the current device (looked up on first use).
-int scratch_address(void **out) {
-    int dev = 0;
+// Device address of g_bwd_scratch on the current device, which must be the plan's.
+int scratch_address(const ta_plan *plan, void **out) {
+    int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
         set_error(std::string("tree_attn_bwd_noalloc: cudaGetDevice: ") + cudaGetErrorString(e));
         return TA_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        set_error("tree_attn_bwd_noalloc: device index beyond the supported range");
-        return TA_ERR_UNSUPPORTED;
+    if (dev != plan->device) {
+        set_error("tree_attn_bwd_noalloc: the plan was built on device " + std::to_string(plan->device) +
+                  " but device " + std::to_string(dev) + " is current");
+        return TA_ERR_INVALID;
     }
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
-        if (e != cudaSuccess || !ptr) {
-            set_error(std::string("tree_attn_bwd_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-            return TA_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = ptr;
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+    if (e != cudaSuccess || !ptr) {
+        set_error(std::string("tree_attn_bwd_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+        return TA_ERR_CUDA;
     }
-    *out = g_scratch_addr[dev];
+    *out = ptr;
     return TA_OK;
 }
 
@@ -80,8 +75,12 @@ extern "C" int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const v
                   " bytes the library holds for this entry point; call tree_attn_bwd with a workspace instead");
         return TA_ERR_UNSUPPORTED;
     }
+    if (plan->device < 0) {
+        set_error("tree_attn_bwd_noalloc: the plan was built with TA_PLAN_HOST_ONLY");
+        return TA_ERR_INVALID;
+    }
     void *scratch = nullptr;
-    const int rc = scratch_address(&scratch);
+    const int rc = scratch_address(plan, &scratch);
     if (rc != TA_OK) return rc;
     return tree_attn_bwd(plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, scratch, kNoAllocScratchBytes,
                          stream);
