@@ -40,7 +40,7 @@ def assert_close(name, got, want, max_abs=MAX_ABS, rel_rms=REL_RMS):
 class Run:
     """One episode on the device: inputs, plan, and the library's outputs."""
 
-    def __init__(self, ep, dist="config", tensors=None, pool=None, dev="cuda:0", flags=0):
+    def __init__(self, ep, dist="config", tensors=None, pool=None, dev="cuda:0", flags=0, **plan_kw):
         self.ep = ep
         self.t = tensors if tensors is not None else W.make_tensors(ep, dist=dist)
         self.pool = pool if pool is not None else W.make_pool(ep, self.t)
@@ -53,7 +53,7 @@ class Run:
         self.plan = ta.tree_attn_plan(ep.branches, ep.mounts, self.pool.page_table,
                                       num_q_heads=Hq, num_kv_heads=ep.num_kv_heads, head_dim=D,
                                       page_size=ep.page_size, num_pages=self.pool.k_pool.shape[0],
-                                      flags=flags)
+                                      flags=flags, **plan_kw)
         self.o = torch.empty((N, Hq, D), dtype=torch.bfloat16, device=self.dev)
         self.lse = torch.empty((Hq, N), dtype=torch.float32, device=self.dev)
 
