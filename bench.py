@@ -41,10 +41,11 @@ DESCRIPTION = {
     0: "tiny tree: 256-row root, 3 x 128-row branches, 1 mount; GQA 4/1, D=64, page 16",
     1: "balanced rollout tree: 4096-row root, fan-out 4 at depth 1 and 2, 2048-row edges; GQA 16/4, D=128, page 64",
     2: "commander-worker DAG: 8192-row root, 8 workers of U[8192,32768] rows, 12 mounts of 1-4 pages; GQA 16/4, D=128, page 64",
-    3: "irregular rollout tree: 64 trajectories, lognormal(7,1) edges, unaligned forks, expanded/compact 6.05; GQA 32/8, D=128, page 64",
+    3: "irregular rollout tree: 64 trajectories, lognormal(7,1) edges, unaligned forks, expanded/compact 5.53; GQA 32/8, D=128, page 64",
     4: "mount-heavy: 4 DAGs x 65,536 rows, 4096-row producer span mounted by 32 readers each; GQA 16/4, D=128, page 64",
 }
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+NOMINAL_BF16_TFLOPS = 2250.0   # GB300 dense bf16 tensor-core peak, nominal (the measured peaks are the denominators)
 KERNEL_SOURCES = {"dkdv": "bwd.cu", "dq": "bwd.cu", "fwd": "fwd.cu"}
 
 
@@ -341,6 +342,74 @@ def run_logprob(args, ep, vocab=151_936):
         "gpu_launches": 3 * args.steps}))
 
 
+def time_workload(name, args, dev, peaks):
+    """Device-resident forward + backward of another workload, timed like the headline (plan
+    reused, inputs resident, CUDA events on the launching stream, per-kernel trace events):
+    its useful TFLOP/s, fractions of the peak and kernel times, for the JSON line."""
+    import torch
+    import dag_packed_paged_gb300 as ta
+    ep = W.config(WORKLOADS[name])
+    t = W.make_tensors(ep)
+    pool = W.make_pool(ep, t)
+    N, Hq, Hkv, D = ep.n_rows, ep.num_q_heads, ep.num_kv_heads, ep.head_dim
+    plan = ta.tree_attn_plan(ep.branches, ep.mounts, pool.page_table, num_q_heads=Hq, num_kv_heads=Hkv,
+                             head_dim=D, page_size=ep.page_size, num_pages=pool.k_pool.shape[0])
+    st = ta.tree_attn_plan_stats(plan)
+    q, k_pool, v_pool, d_o = (bf16_dev(x, dev) for x in (t.q, pool.k_pool, pool.v_pool, t.do))
+    del t, pool
+    o = torch.empty((N, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, N), dtype=torch.float32, device=dev)
+    dq = torch.empty((N, Hq, D), dtype=torch.float32, device=dev)
+    dk_pool = torch.zeros(k_pool.shape, dtype=torch.float32, device=dev)
+    dv_pool = torch.zeros(v_pool.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(ta.tree_attn_bwd_workspace_size(plan), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ta.tree_attn_fwd(plan, q, k_pool, v_pool, o, lse)
+        ta.tree_attn_bwd(plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, ws)
+
+    for _ in range(args.warmup):
+        step()
+    ta.tree_attn_check(plan)
+    K = args.steps
+    trace = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for evs in trace:
+        for e in evs:
+            e.record(stream)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(None, None) as clocks:
+        time.sleep(0.2)
+        ev0.record(stream)
+        for k in range(K):
+            ta.tree_attn_set_trace_events(plan, trace[k])
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    ta.tree_attn_set_trace_events(plan, None)
+    ta.tree_attn_check(plan)
+    ms = ev0.elapsed_time(ev1) / K
+
+    def avg(a, b):
+        return sum(trace[k][a].elapsed_time(trace[k][b]) for k in range(K)) / K
+
+    kern_ms = {"fwd": avg(0, 1), "delta": avg(2, 3), "dq": avg(3, 4), "dkdv": avg(4, 5), "reduce": avg(5, 6)}
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    fwd_tflops = st["fwd_flops"] / kern_ms["fwd"] / 1e9
+    fb_tflops = (st["fwd_flops"] + st["bwd_flops"]) / ms / 1e9
+    out = {"workload": DESCRIPTION[WORKLOADS[name]], "rows": N, "pairs": int(st["pairs"]), "steps": K,
+           "warmup": args.warmup, "ms_per_step": ms, "fwd_tflops": fwd_tflops, "fwdbwd_tflops": fb_tflops,
+           "fwd_frac_of_peak": fwd_tflops / burst, "fwdbwd_frac_of_peak": fb_tflops / burst,
+           "fwd_frac_of_nominal": fwd_tflops / NOMINAL_BF16_TFLOPS,
+           "fwdbwd_frac_of_nominal": fb_tflops / NOMINAL_BF16_TFLOPS,
+           "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()}, "clocks": clocks.summary(),
+           "gpu_launches": K * (1 + 3 + (1 if st["n_partial_slots"] > 0 else 0))}
+    del plan
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -351,6 +420,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clock-log", default=None, help="keep the raw nvidia-smi clock samples in this CSV file")
+    ap.add_argument("--also", default="commander_worker_dag,irregular_tree",
+                    help="comma-separated workloads also timed (device-resident fwd + bwd) at N = 1 and "
+                         "reported under other_workloads; empty for none")
     ap.add_argument("--op", default="attention", choices=["attention", "rope", "logprob"],
                     help="attention: the forward + backward step (the headline); rope: the RoPE kernel alone; "
                          "logprob: compact log-probabilities forward + backward (vocabulary 151,936)")
@@ -548,6 +620,8 @@ def main():
         "data": "synthetic", "config": workload_config(ep, args, st),
         "fwd_tflops": fwd_tflops,
         "fwd_frac_of_peak": fwd_tflops / burst, "fwdbwd_frac_of_peak": value / world / burst,
+        "fwd_frac_of_nominal": fwd_tflops / NOMINAL_BF16_TFLOPS,
+        "fwdbwd_frac_of_nominal": value / world / NOMINAL_BF16_TFLOPS,
         "peak_tflops": {"burst": burst, "sustained": sustained, "kind": peak_kind},
         "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()},
         "plan_ms": statistics.median(plan_times),
@@ -560,6 +634,9 @@ def main():
     }
     if rank == 0:
         line["clocks"] = clocks.summary()
+        others = [w for w in args.also.split(",") if w and w != args.workload] if world == 1 else []
+        if others:
+            line["other_workloads"] = {w: time_workload(w, args, dev, peaks) for w in others}
         if world == 1 and not args.no_cpu_baseline:
             try:
                 line["cpu_baseline"] = cpu_baseline(ep, t)
