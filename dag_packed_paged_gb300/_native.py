@@ -65,7 +65,8 @@ class ta_plan_stats(ctypes.Structure):
                 ("n_kv_tiles", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
                 ("n_partial_slots", ctypes.c_int64), ("block_rows", ctypes.c_int32),
                 ("tile_rows", ctypes.c_int32), ("bwd_workspace_bytes", ctypes.c_size_t),
-                ("plan_ms", ctypes.c_double), ("chunk_cap", ctypes.c_int64), ("num_sms", ctypes.c_int32),
+                ("plan_ms", ctypes.c_double), ("n_ftiles", ctypes.c_int64), ("chunk_cap", ctypes.c_int64),
+                ("num_sms", ctypes.c_int32),
                 ("device", ctypes.c_int32)]
 
 
@@ -78,7 +79,8 @@ class ta_plan_arrays(ctypes.Structure):
                 ("n_intervals", ctypes.c_int64), ("n_entries", ctypes.c_int64),
                 ("n_chunks", ctypes.c_int64), ("pos_ids", _P32), ("blocks", _P32),
                 ("blk_iv_ptr", _P64), ("iv_lo", _P32), ("iv_hi", _P32), ("diag", _P32),
-                ("entries", _P32), ("t_entries", _P32), ("chunks", _P32), ("fwd_order", _P32)]
+                ("entries", _P32), ("t_entries", _P32), ("chunks", _P32), ("fwd_order", _P32),
+                ("n_ftiles", ctypes.c_int64), ("fblk_ptr", _P64), ("ftiles", _P32)]
 
 
 _lib = None
@@ -287,6 +289,8 @@ def tree_attn_plan_export(plan: Plan) -> dict:
         "t_entries": arr(a.t_entries, 4 * ne).reshape(ne, 4),
         "chunks": arr(a.chunks, 4 * a.n_chunks).reshape(a.n_chunks, 4),
         "fwd_order": arr(a.fwd_order, nb),
+        "fblk_ptr": arr(a.fblk_ptr, nb + 1, np.int64),
+        "ftiles": arr(a.ftiles, 8 * a.n_ftiles).reshape(a.n_ftiles, 8),
     }
 
 

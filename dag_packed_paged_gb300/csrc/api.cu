@@ -90,9 +90,12 @@ int make_qtile_map(CUtensorMap *m, const void *base, uint64_t N, uint32_t H, uin
     return TA_OK;
 }
 
-// Tensor maps for Q-like [N, H, D] and the K/V pools.
-int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
-              CUtensorMap *tm_q, CUtensorMap *tm_k, CUtensorMap *tm_v) {
+// Tensor maps for Q-like [N, H, D] and the K/V pools: boxes of one page (the dK/dV kernel's
+// aligned key tiles), of min(page, 32) rows (one slot of a packed key tile) and of 64 rows (two
+// slots that are one aligned run; pages of >= 64 rows only -- otherwise the 32-row map again,
+// which is then never used for a 64-row half).
+int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool, CUtensorMap *tm_q,
+              KvMaps *kv) {
     const HostPlan &h = plan->host;
     const ta_config &c = h.cfg;
     const uint32_t qb = std::min(h.block_rows, 128);
@@ -101,8 +104,14 @@ int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void
     if (rc) return rc;
     const uint64_t pool_rows = uint64_t(c.num_pages) * c.page_size;
     const uint64_t inner = uint64_t(c.num_kv_heads) * c.head_dim;
-    if ((rc = make_map(tm_k, k_pool, inner, pool_rows, inner * 2, 64, c.page_size))) return rc;
-    return make_map(tm_v, v_pool, inner, pool_rows, inner * 2, 64, c.page_size);
+    const uint32_t P = uint32_t(c.page_size), piece = std::min<uint32_t>(P, kPieceRows), half = P >= 64 ? 64 : piece;
+    if ((rc = make_map(&kv->k_page, k_pool, inner, pool_rows, inner * 2, 64, P)) ||
+        (rc = make_map(&kv->v_page, v_pool, inner, pool_rows, inner * 2, 64, P)) ||
+        (rc = make_map(&kv->k_piece, k_pool, inner, pool_rows, inner * 2, 64, piece)) ||
+        (rc = make_map(&kv->v_piece, v_pool, inner, pool_rows, inner * 2, 64, piece)) ||
+        (rc = make_map(&kv->k_half, k_pool, inner, pool_rows, inner * 2, 64, half)))
+        return rc;
+    return make_map(&kv->v_half, v_pool, inner, pool_rows, inner * 2, 64, half);
 }
 
 // Stream-ordered plan upload (TA_PLAN_STREAM_ORDERED).  A copy from pageable memory is staged
@@ -226,13 +235,19 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         size_t bytes;
         size_t off;
     };
-    Part parts[11] = {
+    std::vector<int32_t> fblk(2 * (h.fblk_ptr.size() - 1));
+    for (size_t b = 0; b + 1 < h.fblk_ptr.size(); ++b) {
+        fblk[2 * b] = int32_t(h.fblk_ptr[b]);
+        fblk[2 * b + 1] = int32_t(h.fblk_ptr[b + 1]);
+    }
+    Part parts[13] = {
         {h.blocks.data(), h.blocks.size() * 4, 0},   {h.entries.data(), h.entries.size() * 4, 0},
         {h.t_entries.data(), h.t_entries.size() * 4, 0}, {h.chunks.data(), h.chunks.size() * 4, 0},
         {h.fwd_order.data(), h.fwd_order.size() * 4, 0}, {h.reduce.data(), h.reduce.size() * 4, 0},
         {h.page_table.data(), h.page_table.size() * 4, 0}, {nullptr, 64, 0},
         {h.tile_rows.data(), h.tile_rows.size() * 4, 0}, {h.t_info.data(), h.t_info.size() * 4, 0},
         {h.pos_ids.data(), h.pos_ids.size() * 4, 0},
+        {h.ftiles.data(), h.ftiles.size() * 4, 0},     {fblk.data(), fblk.size() * 4, 0},
     };
     size_t total = 0;
     for (Part &p : parts) {
@@ -280,6 +295,8 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     plan->d_tile_rows = reinterpret_cast<const int32_t *>(d + parts[8].off);
     plan->d_t_info = reinterpret_cast<const int32_t *>(d + parts[9].off);
     plan->d_pos_ids = reinterpret_cast<const int32_t *>(d + parts[10].off);
+    plan->d_ftiles = reinterpret_cast<const int32_t *>(d + parts[11].off);
+    plan->d_fblk = reinterpret_cast<const int32_t *>(d + parts[12].off);
     *out = plan;
     return TA_OK;
 }
@@ -326,6 +343,7 @@ int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out) {
     out->tile_rows = kTileRows;
     out->bwd_workspace_bytes = plan->ws_bytes;
     out->plan_ms = h.plan_ms;
+    out->n_ftiles = int64_t(h.ftiles.size() / kPackInts);
     out->chunk_cap = h.chunk_cap;
     out->num_sms = h.num_sms;
     out->device = plan->device;
@@ -353,6 +371,9 @@ int tree_attn_plan_export(const ta_plan *plan, ta_plan_arrays *out) {
     out->t_entries = h.t_entries.data();
     out->chunks = h.chunks.data();
     out->fwd_order = h.fwd_order.data();
+    out->n_ftiles = int64_t(h.ftiles.size() / kPackInts);
+    out->fblk_ptr = h.fblk_ptr.data();
+    out->ftiles = h.ftiles.data();
     return TA_OK;
 }
 
@@ -493,12 +514,14 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
         set_error("tree_attn_fwd: NULL or misaligned (16-byte) pointer");
         return TA_ERR_INVALID;
     }
-    CUtensorMap tm_q, tm_k, tm_v;
-    int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &tm_k, &tm_v);
+    CUtensorMap tm_q;
+    KvMaps kv;
+    int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &kv);
     if (rc) return rc;
     FwdParams p{};
     p.blocks = plan->d_blocks;
-    p.entries = plan->d_entries;
+    p.ftiles = plan->d_ftiles;
+    p.fblk = plan->d_fblk;
     p.order = plan->d_fwd_order;
     p.page_table = plan->d_page_table;
     p.tile_rows = plan->d_tile_rows;
@@ -514,7 +537,7 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.status = plan->d_status;
-    cudaError_t e = launch_fwd(h.cfg.head_dim, tm_q, tm_k, tm_v, p, int(h.blocks.size() / 4),
+    cudaError_t e = launch_fwd(h.cfg.head_dim, tm_q, kv, p, int(h.blocks.size() / 4),
                                static_cast<cudaStream_t>(stream), plan->trace);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
     return TA_OK;
@@ -540,8 +563,9 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
         set_error("tree_attn_bwd: workspace too small or not 256-byte aligned");
         return TA_ERR_INVALID;
     }
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;
-    int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &tm_k, &tm_v);
+    CUtensorMap tm_q, tm_do;
+    KvMaps kv;
+    int rc = make_maps(plan, q, k_pool, v_pool, &tm_q, &kv);
     if (rc) return rc;
     const ta_config &c = h.cfg;
     // the backward loads Q and dO a whole 128-lane tile per box
@@ -551,7 +575,8 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
         return rc;
     BwdParams p{};
     p.blocks = plan->d_blocks;
-    p.entries = plan->d_entries;
+    p.ftiles = plan->d_ftiles;
+    p.fblk = plan->d_fblk;
     p.t_entries = plan->d_t_entries;
     p.chunks = plan->d_chunks;
     p.reduce = plan->d_reduce;
@@ -582,7 +607,7 @@ int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.dk_pool = dk_pool;
     p.dv_pool = dv_pool;
     p.status = plan->d_status + 1;
-    cudaError_t e = launch_bwd(c.head_dim, tm_q, tm_k, tm_v, tm_do, p, int(h.blocks.size() / 4),
+    cudaError_t e = launch_bwd(c.head_dim, tm_q, kv, tm_do, p, int(h.blocks.size() / 4),
                                int(h.chunks.size() / 4), int(h.reduce.size() / 4), static_cast<cudaStream_t>(stream),
                                plan->trace);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attn_bwd launch");

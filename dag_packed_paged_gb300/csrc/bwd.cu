@@ -10,7 +10,7 @@
 //   delta_kernel   per (query block, KV head, 128-lane query tile): each lane's -lse * log2(e)
 //                  and -delta = -<dO, O>, one 1 KB table per tile              (HBM-bound)
 //   dq_kernel      query-major: one CTA per (query block, KV head, 128-lane query tile);
-//                  walks the block's key-tile entries like the forward
+//                  walks the block's packed key tiles like the forward
 //   dkdv_kernel    key-major: one CTA per (key-tile chunk, KV head); walks the query blocks
 //                  that read the tile (the plan's transpose), both 128-lane query tiles each;
 //                  dK and dV accumulate in TMEM and are written once -- to the pool, or to a
@@ -187,7 +187,8 @@ struct DqLayout {
 template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k64,
+          const __grid_constant__ CUtensorMap tm_v64, const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
     using L = DqLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -197,8 +198,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const int unit = blockIdx.x >> 1, t = blockIdx.x & 1;
     const int qb = __ldg(p.order + unit / p.Hkv), g = unit % p.Hkv;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
-    const int e0 = __ldg(p.blocks + 4 * qb + 2), E = __ldg(p.blocks + 4 * qb + 3) - e0;
-    const int4 *entries = reinterpret_cast<const int4 *>(p.entries) + e0;
+    const int e0 = __ldg(p.fblk + 2 * qb), E = __ldg(p.fblk + 2 * qb + 1) - e0;
+    const int4 *tiles = reinterpret_cast<const int4 *>(p.ftiles) + 2 * e0;   // two int4 per tile
 
     const uint32_t sK = sbase + L::k_off, sV = sbase + L::v_off, sDO = sbase + L::do_off;
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
@@ -242,37 +243,40 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     constexpr uint32_t cQ = 0, cDS = 64, cDQ = 128, cS = 256, cDP = 384;
 
     if (warp == 8) {
-        const int ppt = kTileRows / p.page_size;
         bool do_issued = false;
         if (lane == 0) {
             tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_k64); tma_prefetch_desc(&tm_v64);
             if (E > 0) {
                 mbar_arrive_expect_tx(do_full, L::kTile);
                 load_q_tile(sDO, &tm_do, t, g, p.G, p.R, q_row0, do_full);
                 do_issued = true;
             }
         }
-        EntryFeed f;
+        PackFeed f;
+        const int oob = p.num_pages * p.page_size;
         int k_issued = 0, v_issued = 0;
         for (int j = 0; j < E; ++j) {
-            if ((j & 31) == 0) feed_fill(f, j, E, entries, p.tile_rows, ppt, lane);
+            if ((j & 31) == 0)
+                pack_feed_fill(f, j, E, tiles, p.page_table, p.n_logical_pages, p.page_size, oob, lane);
             int y[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, f.y[i], j & 31);
+            const int fl = __shfl_sync(0xffffffffu, f.b.z, j & 31);
             const int ks = j % kKStages, vs = j % kVStages;
             bool ok = true;
             if (lane == 0 && j >= kKStages) ok = mbar_wait(k_empty(ks), ((j / kKStages) - 1) & 1, abort, p.status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(k_full(ks), L::kTile);
-                tma_kv_tile(sK + ks * L::kTile, &tm_k, y, ppt, p.page_size, g, D, k_full(ks));
+                tma_packed_tile(sK + ks * L::kTile, &tm_k, &tm_k64, y, fl, p.page_size, g, D, k_full(ks));
             }
             k_issued = j + 1;
             if (lane == 0 && j >= kVStages) ok = mbar_wait(v_empty(vs), ((j / kVStages) - 1) & 1, abort, p.status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(v_full(vs), L::kTile);
-                tma_kv_tile(sV + vs * L::kTile, &tm_v, y, ppt, p.page_size, g, D, v_full(vs));
+                tma_packed_tile(sV + vs * L::kTile, &tm_v, &tm_v64, y, fl, p.page_size, g, D, v_full(vs));
             }
             v_issued = j + 1;
         }
@@ -358,9 +362,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const float nlse2 = tab[32 * q4 + lane];      // -lse * log2(e)
         const float ndelta = tab[128 + 32 * q4 + lane];  // -delta
         bool ok = true;
-        WarpRecords recs;
+        WarpPackRecords recs;
         for (int j = 0; j < E; ++j) {
-            const int4 e = recs.get(entries, j, E, lane);
+            int4 ra, rb;
+            recs.get(tiles, j, E, lane, ra, rb);
             // ---------------- phase 1: P_j from S_j
             ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort, p.status));
             if (!ok) break;
@@ -382,12 +387,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                     pf[2 * i] = ex2(x0);
                     pf[2 * i + 1] = ex2(x1);
                 }
-                if (e.w != 0) {                      // partial / diagonal tile: mask key columns
-                    const int j0 = e.x * kTileRows + 64 * w;
-                    const int lo = e.y - j0;
-                    const int hi = ((e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z) - j0;
+                if (rb.z & kPackMask) {              // this group's slots 2w, 2w + 1: mask key columns
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) pf[i] = (i >= lo && i < hi) ? pf[i] : 0.f;
+                    for (int sl = 0; sl < 2; ++sl) {
+                        int lo, hi;
+                        pack_slot_range(ra, rb, 2 * w + sl, r_abs, lo, hi);
+                        if (lo > 0 || hi < kPieceRows) {
+#pragma unroll
+                            for (int c = 0; c < kPieceRows; ++c)
+                                pf[kPieceRows * sl + c] = (c >= lo && c < hi) ? pf[kPieceRows * sl + c] : 0.f;
+                        }
+                    }
                 }
             }
             // ---------------- phase 2: dS_j
@@ -820,9 +830,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(const BwdParams p) {
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                         const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
-                         cudaStream_t stream, void *const *trace) {
+cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const KvMaps &kv, const CUtensorMap &tm_do, const BwdParams &p,
+                         int n_blocks, int n_chunks, int n_reduce, cudaStream_t stream, void *const *trace) {
     trace_record(trace, 2, stream);
     delta_kernel<D><<<static_cast<unsigned>(n_blocks) * p.Hkv * 2, 128, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
@@ -830,12 +839,14 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
     e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::bytes);
     if (e != cudaSuccess) return e;
     trace_record(trace, 3, stream);
-    dq_kernel<D><<<n_blocks * p.Hkv * 2, kDqThreads, DqLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    dq_kernel<D><<<n_blocks * p.Hkv * 2, kDqThreads, DqLayout<D>::bytes, stream>>>(
+        tm_q, kv.k_piece, kv.v_piece, kv.k_half, kv.v_half, tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::bytes);
     if (e != cudaSuccess) return e;
     trace_record(trace, 4, stream);
-    dkdv_kernel<D><<<n_chunks * p.Hkv, kDkvThreads, DkvLayout<D>::bytes, stream>>>(tm_q, tm_k, tm_v, tm_do, p);
+    dkdv_kernel<D><<<n_chunks * p.Hkv, kDkvThreads, DkvLayout<D>::bytes, stream>>>(tm_q, kv.k_page, kv.v_page,
+                                                                                    tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     trace_record(trace, 5, stream);
     if (n_reduce > 0) {
@@ -848,11 +859,11 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
 
 }  // namespace
 
-cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks, int n_reduce,
-                       cudaStream_t stream, void *const *trace) {
-    if (D == 64) return launch_bwd_d<64>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream, trace);
-    return launch_bwd_d<128>(tm_q, tm_k, tm_v, tm_do, p, n_blocks, n_chunks, n_reduce, stream, trace);
+cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const CUtensorMap &tm_do,
+                       const BwdParams &p, int n_blocks, int n_chunks, int n_reduce, cudaStream_t stream,
+                       void *const *trace) {
+    if (D == 64) return launch_bwd_d<64>(tm_q, kv, tm_do, p, n_blocks, n_chunks, n_reduce, stream, trace);
+    return launch_bwd_d<128>(tm_q, kv, tm_do, p, n_blocks, n_chunks, n_reduce, stream, trace);
 }
 
 }  // namespace treeattn

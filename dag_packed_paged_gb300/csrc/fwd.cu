@@ -3,15 +3,17 @@
 // Computes, for every row r of one query block and the G query heads of one KV head g,
 //   O[r,h] = sum_{j in vis(r)} softmax_j(scale q[r,h].k[j,g]) v[j,g],   lse[h,r] = ln sum exp
 // (Octopus arXiv 2611.06956 Section 3.3 Eq. 4 with the rectangular causal alignment after it;
-// HARTS arXiv 2608.28158 Section 4.2 Eq. 21-22), visiting only the key tiles the plan lists
-// for the block and masking rows outside each entry's [lo, hi) and, on diagonal tiles, above
-// the query row.
+// HARTS arXiv 2608.28158 Section 4.2 Eq. 21-22), visiting only the packed key tiles the plan
+// lists for the block -- 4 slots of 32 key rows each, gathered from the visible intervals --
+// and masking each slot's rows outside its [lo, hi) and, on slots of the block's own rows,
+// above the query row.
 //
 // One CTA = one query block (R rows x G heads = 256 query rows of the MMA, two 128-lane
 // tiles) x one KV head.  Warp roles:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one (row, head) per thread)
 //   warps 4-7  softmax for query tile 1
-//   warp 8     TMA producer: Q once, then K and V tiles page by page (box = one page)
+//   warp 8     TMA producer: Q once, then K and V tiles slot by slot (a box per 32-row slot,
+//              or per 64-row half when its two slots are one aligned run)
 //   warp 9     tcgen05 MMA issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P read from TMEM
 // TMEM (512 columns): S0 | S1 | O0 | O1; P_t (bf16 pairs) overwrites the first half of S_t.
 // The two query tiles ping-pong so that one tile's softmax overlaps the other tile's MMAs.
@@ -43,23 +45,11 @@ struct FwdLayout {
     static constexpr int bytes = misc_off + 16 + 1024;     // + alignment slack
 };
 
-// TMA: one K or V tile (kTileRows rows of KV head g) of logical tile `tile`, page by page.
-__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap *tm, int tile, int g,
-                                             int D, const int32_t *page_table, int n_logical,
-                                             int num_pages, int P, uint32_t bar) {
-    const int pages = kTileRows / P;
-    for (int i = 0; i < pages; ++i) {
-        const int l = tile * pages + i;
-        const int y = l < n_logical ? __ldg(page_table + l) * P : num_pages * P;   // past the end: zero fill
-        for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(dst + c * (kTileRows * 128) + i * P * 128, tm, g * D + c * 64, y, bar);
-    }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k64,
+           const __grid_constant__ CUtensorMap tm_v64, const FwdParams p) {
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -69,8 +59,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int qb = __ldg(p.order + blockIdx.x / p.Hkv);
     const int g = blockIdx.x % p.Hkv;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
-    const int e0 = __ldg(p.blocks + 4 * qb + 2), E = __ldg(p.blocks + 4 * qb + 3) - e0;
-    const int4 *entries = reinterpret_cast<const int4 *>(p.entries) + e0;
+    const int e0 = __ldg(p.fblk + 2 * qb), E = __ldg(p.fblk + 2 * qb + 1) - e0;
+    const int4 *tiles = reinterpret_cast<const int4 *>(p.ftiles) + 2 * e0;   // two int4 per tile
 
     const uint32_t sQ = sbase + L::q_off, sK = sbase + L::k_off, sV = sbase + L::v_off;
     auto bar = [&](int i) { return sbase + L::bar_off + 8u * i; };
@@ -109,6 +99,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_k64);
+            tma_prefetch_desc(&tm_v64);
             const int R = p.R, QB = R < 128 ? R : 128;
             mbar_arrive_expect_tx(q_full, 2 * L::kQTile);
             for (int t = 0; t < 2; ++t)
@@ -118,21 +110,36 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         tma_load_2d(sQ + t * L::kQTile + c * 16384 + b * QB * 128, &tm_q,
                                     (g * p.G + hl) * D + c * 64, q_row0 + r0, q_full);
                 }
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < E; ++j) {
-                const int tile = __ldg(&entries[j].x);
-                const int ks = j % kKS, vs = j % kVS;
-                if (j >= kKS && !mbar_wait(k_empty(ks), ((j / kKS) - 1) & 1, abort, p.status)) break;
+        }
+        // the whole warp prefetches tile records and TMA rows 32 tiles at a time; lane 0 issues
+        PackFeed f;
+        const int oob = p.num_pages * p.page_size;
+        int k_issued = 0, v_issued = 0;
+        for (int j = 0; j < E; ++j) {
+            if ((j & 31) == 0)
+                pack_feed_fill(f, j, E, tiles, p.page_table, p.n_logical_pages, p.page_size, oob, lane);
+            int y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, f.y[i], j & 31);
+            const int fl = __shfl_sync(0xffffffffu, f.b.z, j & 31);
+            const int ks = j % kKS, vs = j % kVS;
+            bool ok = true;
+            if (lane == 0 && j >= kKS) ok = mbar_wait(k_empty(ks), ((j / kKS) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(k_full(ks), L::kKV);
-                load_kv_tile(sK + ks * L::kKV, &tm_k, tile, g, D, p.page_table, p.n_logical_pages,
-                             p.num_pages, p.page_size, k_full(ks));
-                k_issued = j + 1;
-                if (j >= kVS && !mbar_wait(v_empty(vs), ((j / kVS) - 1) & 1, abort, p.status)) break;
-                mbar_arrive_expect_tx(v_full(vs), L::kKV);
-                load_kv_tile(sV + vs * L::kKV, &tm_v, tile, g, D, p.page_table, p.n_logical_pages,
-                             p.num_pages, p.page_size, v_full(vs));
-                v_issued = j + 1;
+                tma_packed_tile(sK + ks * L::kKV, &tm_k, &tm_k64, y, fl, p.page_size, g, D, k_full(ks));
             }
+            k_issued = j + 1;
+            if (lane == 0 && j >= kVS) ok = mbar_wait(v_empty(vs), ((j / kVS) - 1) & 1, abort, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(v_full(vs), L::kKV);
+                tma_packed_tile(sV + vs * L::kKV, &tm_v, &tm_v64, y, fl, p.page_size, g, D, v_full(vs));
+            }
+            v_issued = j + 1;
+        }
+        if (lane == 0) {
             // never leave the CTA with copies in flight: wait for the last phase of each stage
             for (int d = (k_issued > kKS ? k_issued - kKS : 0); d < k_issued; ++d)
                 mbar_wait(k_full(d % kKS), (d / kKS) & 1, nullptr, p.status);
@@ -209,9 +216,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        WarpRecords recs;
+        WarpPackRecords recs;
         for (int j = 0; j < E; ++j) {
-            const int4 e = recs.get(entries, j, E, lane);
+            int4 ra, rb;
+            recs.get(tiles, j, E, lane, ra, rb);
             ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, abort, p.status));
             if (!ok) break;                          // warp-uniform: tcgen05.ld/st are collective
             tc_fence_after();
@@ -223,13 +231,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             float s[kTileRows];
 #pragma unroll
             for (int c = 0; c < kTileRows; ++c) s[c] = __uint_as_float(sb[c]);
-            if (e.w != 0) {
-                const int j0 = e.x * kTileRows;
-                const int hi = (e.w & kEntryCausal) ? min(e.z, r_abs + 1) : e.z;
+            if (rb.z & kPackMask) {                   // some slot is partial, causal or empty
 #pragma unroll
-                for (int c = 0; c < kTileRows; ++c) {
-                    const int jj = j0 + c;
-                    if (jj < e.y || jj >= hi) s[c] = -INFINITY;
+                for (int k = 0; k < 4; ++k) {
+                    int lo, hi;
+                    pack_slot_range(ra, rb, k, r_abs, lo, hi);
+                    if (lo > 0 || hi < kPieceRows) {
+#pragma unroll
+                        for (int c = 0; c < kPieceRows; ++c)
+                            if (c < lo || c >= hi) s[kPieceRows * k + c] = -INFINITY;
+                    }
                 }
             }
             // row max: a tree of three-input maxima (16 independent chains, then a final fold)
@@ -331,13 +342,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 }
 
 template <int D>
-cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                         const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace) {
+cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
+                         cudaStream_t stream, void *const *trace) {
     const int smem = FwdLayout<D>::bytes;
     cudaError_t err = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     trace_record(trace, 0, stream);
-    fwd_kernel<D><<<n_blocks * p.Hkv, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
+    fwd_kernel<D><<<n_blocks * p.Hkv, kThreads, smem, stream>>>(tm_q, kv.k_piece, kv.v_piece, kv.k_half,
+                                                                 kv.v_half, p);
     err = cudaGetLastError();
     trace_record(trace, 1, stream);
     return err;
@@ -345,10 +357,10 @@ cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
 
 }  // namespace
 
-cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace) {
-    if (D == 64) return launch_fwd_d<64>(tm_q, tm_k, tm_v, p, n_blocks, stream, trace);
-    return launch_fwd_d<128>(tm_q, tm_k, tm_v, p, n_blocks, stream, trace);
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
+                       cudaStream_t stream, void *const *trace) {
+    if (D == 64) return launch_fwd_d<64>(tm_q, kv, p, n_blocks, stream, trace);
+    return launch_fwd_d<128>(tm_q, kv, p, n_blocks, stream, trace);
 }
 
 }  // namespace treeattn

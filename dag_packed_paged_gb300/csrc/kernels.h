@@ -10,7 +10,8 @@ namespace treeattn {
 
 struct FwdParams {
     const int32_t *blocks;      // 4 per query block: first row, rows, entry begin, entry end
-    const int32_t *entries;     // 4 per entry: key tile, lo, hi, flags
+    const int32_t *ftiles;      // packed key tiles, kPackInts each (plan.h)
+    const int32_t *fblk;        // per query block: first packed tile, end
     const int32_t *order;       // query blocks, longest first
     const int32_t *page_table;  // logical page -> pool page
     const int32_t *tile_rows;   // per key tile, per page: pool row of the page (TMA y)
@@ -27,7 +28,8 @@ struct FwdParams {
 
 struct BwdParams {
     const int32_t *blocks;
-    const int32_t *entries;
+    const int32_t *ftiles;      // packed key tiles of the dQ kernel (as the forward's)
+    const int32_t *fblk;
     const int32_t *t_entries;   // 4 per entry, key-tile-major: block, lo, hi, flags
     const int32_t *chunks;      // 4 per chunk: tile, t_entry begin, end, partial slot
     const int32_t *reduce;      // 4 per split tile: tile, first slot, slots, 0
@@ -78,12 +80,19 @@ cudaError_t launch_logprob_bwd(const __nv_bfloat16 *z, int64_t C, int64_t V, con
                                const int64_t *row_pos, const int32_t *pos_target, const float *g, __nv_bfloat16 *dz,
                                cudaStream_t stream);
 
-cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const FwdParams &p, int n_blocks, cudaStream_t stream, void *const *trace);
+// Tensor maps of the K/V pools: `page` boxes of one page (the dK/dV kernel's aligned tiles),
+// `piece` boxes of min(page, 32) rows and `half` boxes of 64 rows (packed tiles of the forward
+// and dQ; `half` is only used when pages hold >= 64 rows).
+struct KvMaps {
+    CUtensorMap k_page, v_page, k_piece, v_piece, k_half, v_half;
+};
 
-cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const CUtensorMap &tm_do, const BwdParams &p, int n_blocks, int n_chunks,
-                       int n_reduce, cudaStream_t stream, void *const *trace);
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
+                       cudaStream_t stream, void *const *trace);
+
+cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const CUtensorMap &tm_do,
+                       const BwdParams &p, int n_blocks, int n_chunks, int n_reduce, cudaStream_t stream,
+                       void *const *trace);
 
 inline void trace_record(void *const *trace, int i, cudaStream_t s) {
     if (trace && trace[i]) cudaEventRecord(static_cast<cudaEvent_t>(trace[i]), s);

@@ -51,6 +51,69 @@ int fail(int code, const std::string &msg) {
     return code;
 }
 
+// Packs one query block's visible key rows into tiles of 4 slots x 32 rows (see plan.h).
+// `items`: the block's visible intervals, the own-rows run flagged causal; r0: its first row.
+// Every interval is cut into 32-row-aligned pieces; an even piece followed by the next one
+// forms a 64-row half (one TMA box when pages hold >= 64 rows), the other pieces pair up into
+// halves of two single boxes; halves fill tiles in order.  Rows outside the block's visible
+// set occupy only the uncovered ends of pieces and the empty slot of a last half or tile.
+void pack_block_tiles(const std::vector<std::pair<Interval, bool>> &items, int64_t r0, bool half_boxes,
+                      std::vector<int32_t> &out) {
+    struct Piece {
+        int64_t q;
+        int32_t lo, hi;
+        bool causal;
+    };
+    std::vector<Piece> pcs;
+    for (const auto &it : items) {
+        const Interval x = it.first;
+        for (int64_t q = x.lo / kPieceRows; q * kPieceRows < x.hi; ++q) {
+            const int64_t a = std::max<int64_t>(x.lo, q * kPieceRows), z = std::min<int64_t>(x.hi, (q + 1) * kPieceRows);
+            pcs.push_back({q, int32_t(a - q * kPieceRows), int32_t(z - q * kPieceRows), it.second && z - 1 > r0});
+        }
+    }
+    std::stable_sort(pcs.begin(), pcs.end(), [](const Piece &a, const Piece &b) {
+        return a.q < b.q || (a.q == b.q && a.lo < b.lo);
+    });
+    const Piece none{-1, 0, 0, false};
+    std::vector<std::array<Piece, 2>> halves;
+    std::vector<bool> joined;                 // the half is one 64-row-aligned run
+    const Piece *single = nullptr;
+    for (size_t i = 0; i < pcs.size(); ++i) {
+        if (pcs[i].q % 2 == 0 && i + 1 < pcs.size() && pcs[i + 1].q == pcs[i].q + 1) {
+            halves.push_back({pcs[i], pcs[i + 1]});
+            joined.push_back(half_boxes);
+            ++i;
+        } else if (single) {
+            halves.push_back({*single, pcs[i]});
+            joined.push_back(false);
+            single = nullptr;
+        } else {
+            single = &pcs[i];
+        }
+    }
+    if (single) {
+        halves.push_back({*single, none});
+        joined.push_back(false);
+    }
+    for (size_t h = 0; h < halves.size(); h += 2) {
+        Piece s[4] = {halves[h][0], halves[h][1], none, none};
+        int32_t flags = joined[h] ? kPackHalf64 : 0;
+        if (h + 1 < halves.size()) {
+            s[2] = halves[h + 1][0];
+            s[3] = halves[h + 1][1];
+            if (joined[h + 1]) flags |= kPackHalf64 << 1;
+        }
+        for (int k = 0; k < 4; ++k) {
+            if (s[k].causal) flags |= kPackCausal << k;
+            if (s[k].q < 0 || s[k].lo != 0 || s[k].hi != kPieceRows || s[k].causal) flags |= kPackMask;
+        }
+        out.insert(out.end(), {int32_t(s[0].q), int32_t(s[1].q), int32_t(s[2].q), int32_t(s[3].q),
+                               s[0].lo | s[0].hi << 6 | s[1].lo << 12 | s[1].hi << 18,
+                               s[2].lo | s[2].hi << 6 | s[3].lo << 12 | s[3].hi << 18, flags, 0});
+    }
+}
+
 }  // namespace
 
 int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts,
@@ -357,6 +420,7 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
     const int64_t n_blocks = (int64_t)blocks.size() / 4;
 
     // ------------------------------------------------------------------ key-tile entries
+    P.fblk_ptr.assign(1, 0);
     for (int64_t qb = 0; qb < n_blocks; ++qb) {
         const int64_t r0 = blocks[4 * qb];
         blocks[4 * qb + 2] = (int32_t)(P.entries.size() / 4);
@@ -382,14 +446,16 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
             }
         }
         blocks[4 * qb + 3] = (int32_t)(P.entries.size() / 4);
+        pack_block_tiles(items, r0, Pg >= 64, P.ftiles);
+        P.fblk_ptr.push_back((int64_t)(P.ftiles.size() / kPackInts));
     }
     const int64_t n_entries = (int64_t)P.entries.size() / 4;
 
-    // launch order for query-major kernels: most entries first (LPT)
+    // launch order for query-major kernels: most packed tiles first (LPT)
     P.fwd_order.resize(n_blocks);
     std::iota(P.fwd_order.begin(), P.fwd_order.end(), 0);
     std::stable_sort(P.fwd_order.begin(), P.fwd_order.end(), [&](int32_t a, int32_t b) {
-        return blocks[4 * a + 3] - blocks[4 * a + 2] > blocks[4 * b + 3] - blocks[4 * b + 2];
+        return P.fblk_ptr[a + 1] - P.fblk_ptr[a] > P.fblk_ptr[b + 1] - P.fblk_ptr[b];
     });
 
     // ------------------------------------------------------------------ transpose (tile-major)

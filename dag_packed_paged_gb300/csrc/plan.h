@@ -15,6 +15,22 @@ constexpr int kBlockMRows = 256;     // query (row, head) pairs per query block:
 constexpr int32_t kEntryCausal = 1;  // mask key rows above the query row
 constexpr int32_t kEntryPartial = 2; // the entry covers only part of its tile
 
+// Packed key tiles of the query-major kernels (forward, dQ): a tile is 4 slots of 32 key rows,
+// each slot one 32-row-aligned piece of the strip that the block sees in part or in full, so
+// that the pieces of several visible intervals share one 128-row tile.  Record (8 x int32):
+//   [0..3] piece index (first row / 32) of slot k, -1 for an empty slot
+//   [4]    slots 0, 1: lo | hi << 6 | lo << 12 | hi << 18   (visible rows [lo, hi) of the piece)
+//   [5]    slots 2, 3, the same
+//   [6]    flags: kPackMask (some slot needs masking), kPackCausal << k (slot k: mask rows
+//          above the query row), kPackHalf64 << h (slots 2h, 2h+1 are one 64-row-aligned run,
+//          loaded as one box)
+//   [7]    0
+constexpr int kPieceRows = 32;
+constexpr int kPackInts = 8;
+constexpr int32_t kPackMask = 1;
+constexpr int32_t kPackCausal = 2;    // bits 1..4
+constexpr int32_t kPackHalf64 = 32;   // bits 5..6
+
 void set_error(const std::string &msg);
 
 struct HostPlan {
@@ -39,6 +55,8 @@ struct HostPlan {
     std::vector<int32_t> tile_rows;   // per key tile, per page: TMA row of the page in the pool
                                       // (pool rows; num_pages * P past the strip: zero fill)
     std::vector<int32_t> t_info;      // per tile-major entry: block << 2 | flags, first row, lo, hi
+    std::vector<int32_t> ftiles;      // packed key tiles of the query-major kernels (kPackInts each)
+    std::vector<int64_t> fblk_ptr;    // n_blocks + 1: block b's packed tiles [fblk_ptr[b], fblk_ptr[b+1])
     int64_t n_segments = 0;
     int64_t n_partial_slots = 0;
     int64_t chunk_cap = 0;            // entries per dK/dV chunk at most
@@ -72,6 +90,8 @@ struct ta_plan {
     const int32_t *d_tile_rows = nullptr;
     const int32_t *d_t_info = nullptr;
     const int32_t *d_pos_ids = nullptr;   // Eq. 2 position of every compact row
+    const int32_t *d_ftiles = nullptr;    // packed key tiles (forward, dQ)
+    const int32_t *d_fblk = nullptr;      // per block: first packed tile, end (2 x int32)
     int32_t *d_status = nullptr;      // bounded-wait status words (zeroed at plan time)
     size_t ws_table_bytes = 0;        // workspace: per (KV head, block, query tile) 128 lse*log2e + 128 delta
     size_t ws_bytes = 0;              // total bwd workspace

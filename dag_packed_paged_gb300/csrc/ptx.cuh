@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "plan.h"
+
 namespace treeattn {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait, then give up
@@ -302,6 +304,79 @@ __device__ __forceinline__ void tma_kv_tile(uint32_t dst, const void *tm, const 
                 tma_load_2d(dst + c * (128 * 128) + i * P * 128, tm, g * D + c * 64, y[i], bar);
 }
 
+// Warp-cooperative prefetch of packed key tiles (the forward's and dQ's tile lists): lane i
+// holds the record of tile (base + i) and the TMA row of every box it loads, so one round trip
+// serves 32 tiles.  A tile has 4 slots of 32 key rows; slot k's rows are box y[2k] (and, for
+// 16-row pages, y[2k + 1]).  An empty slot, or the second 16-row half of a piece past the last
+// logical page, reads row `oob_row` (past the pool: TMA fills zeros).
+struct PackFeed {
+    int4 a;      // slot pieces (first row / 32), -1 empty
+    int4 b;      // slot row ranges and flags
+    int y[8];
+};
+
+__device__ __forceinline__ void pack_feed_fill(PackFeed &f, int base, int n, const int4 *tiles,
+                                               const int32_t *page_table, int n_logical, int P, int oob_row,
+                                               int lane) {
+    const int j = base + lane;
+    if (j < n) {
+        f.a = __ldg(tiles + 2 * j);
+        f.b = __ldg(tiles + 2 * j + 1);
+        const int pc[4] = {f.a.x, f.a.y, f.a.z, f.a.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int p = pc[k];
+            if (P >= 32) {
+                f.y[2 * k] = p >= 0 ? __ldg(page_table + (32 * p) / P) * P + (32 * p) % P : oob_row;
+                f.y[2 * k + 1] = oob_row;
+            } else {   // 16-row pages: a piece is two pages
+                f.y[2 * k] = p >= 0 ? __ldg(page_table + 2 * p) * P : oob_row;
+                f.y[2 * k + 1] = (p >= 0 && 2 * p + 1 < n_logical) ? __ldg(page_table + 2 * p + 1) * P : oob_row;
+            }
+        }
+    }
+}
+
+// TMA loads of one packed key tile of KV head g into a 128-row smem tile (slot k at rows
+// [32k, 32k + 32), each 64-column chunk c in its own 16 KB part).  `tm_s`: boxes of
+// min(P, 32) rows; `tm_h`: boxes of 64 rows, used for a half whose two slots are one
+// 64-row-aligned run (flag bit kPackHalf64 << h; pages of >= 64 rows).  Always 128 * D * 2
+// bytes in total.
+__device__ __forceinline__ void tma_packed_tile(uint32_t dst, const void *tm_s, const void *tm_h, const int (&y)[8],
+                                                int flags, int P, int g, int D, uint32_t bar) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (flags & (kPackHalf64 << h)) {
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_2d(dst + c * (128 * 128) + h * 64 * 128, tm_h, g * D + c * 64, y[4 * h], bar);
+        } else {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const int k = 2 * h + s;
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_2d(dst + c * (128 * 128) + k * 32 * 128, tm_s, g * D + c * 64, y[2 * k], bar);
+                    if (P < 32)
+                        tma_load_2d(dst + c * (128 * 128) + k * 32 * 128 + 16 * 128, tm_s, g * D + c * 64,
+                                    y[2 * k + 1], bar);
+                }
+            }
+        }
+    }
+}
+
+// Visible columns [lo, hi) of slot k of a packed tile for query row r: the slot's row range,
+// cut above r when the slot is causal.  rec_a: slot pieces, rec_b: ranges and flags.
+__device__ __forceinline__ void pack_slot_range(const int4 &rec_a, const int4 &rec_b, int k, int r, int &lo,
+                                                int &hi) {
+    const uint32_t w = static_cast<uint32_t>(k < 2 ? rec_b.x : rec_b.y) >> (12 * (k & 1));
+    lo = static_cast<int>(w & 63u);
+    hi = static_cast<int>((w >> 6) & 63u);
+    if (rec_b.z & (kPackCausal << k)) {
+        const int p = k == 0 ? rec_a.x : k == 1 ? rec_a.y : k == 2 ? rec_a.z : rec_a.w;
+        hi = min(hi, r + 1 - 32 * p);
+    }
+}
+
 // Per-warp broadcast of a list of int4 records (plan entries): lane i holds record (base + i);
 // one coalesced load serves 32 iterations and every iteration reads its record by shuffle,
 // so no global-memory latency sits on the per-iteration critical path.
@@ -312,6 +387,22 @@ struct WarpRecords {
         const int src = i & 31;
         return make_int4(__shfl_sync(0xffffffffu, mine.x, src), __shfl_sync(0xffffffffu, mine.y, src),
                          __shfl_sync(0xffffffffu, mine.z, src), __shfl_sync(0xffffffffu, mine.w, src));
+    }
+};
+
+// The same for packed key tiles (two int4 per record).
+struct WarpPackRecords {
+    int4 a = make_int4(0, 0, 0, 0), b = make_int4(0, 0, 0, 0);
+    __device__ __forceinline__ void get(const int4 *tiles, int i, int n, int lane, int4 &ra, int4 &rb) {
+        if ((i & 31) == 0 && i + lane < n) {
+            a = __ldg(tiles + 2 * (i + lane));
+            b = __ldg(tiles + 2 * (i + lane) + 1);
+        }
+        const int src = i & 31;
+        ra = make_int4(__shfl_sync(0xffffffffu, a.x, src), __shfl_sync(0xffffffffu, a.y, src),
+                       __shfl_sync(0xffffffffu, a.z, src), __shfl_sync(0xffffffffu, a.w, src));
+        rb = make_int4(__shfl_sync(0xffffffffu, b.x, src), __shfl_sync(0xffffffffu, b.y, src),
+                       __shfl_sync(0xffffffffu, b.z, src), 0);
     }
 };
 

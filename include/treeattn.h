@@ -137,6 +137,7 @@ typedef struct {
     int32_t tile_rows;       /* key rows per tile (128) */
     size_t bwd_workspace_bytes;
     double plan_ms;          /* host time spent in tree_attn_plan */
+    int64_t n_ftiles;        /* packed key tiles of the forward and dQ kernels */
     int64_t chunk_cap;       /* entries per dK/dV chunk at most (see ta_config) */
     int32_t num_sms;         /* SM count the chunk cap was derived from */
     int32_t device;          /* CUDA device the plan was uploaded to (-1: host-only plan) */
@@ -154,7 +155,15 @@ typedef struct {
  *   t_entries[4*n_entries]             key-tile-major {block, lo, hi, flags}
  *   chunks[4*n_chunks]                 {key tile, first t_entry, end t_entry, partial slot or -1}
  *   fwd_order[n_blocks]                order in which query blocks are launched
- * flags: bit 0 = causal (mask j > r), bit 1 = the entry does not cover its whole tile. */
+ *   fblk_ptr[n_blocks+1], ftiles[8*n_ftiles]
+ *                                      per block: the packed key tiles the forward and dQ
+ *                                      kernels visit -- 4 slots of 32 key rows each:
+ *                                      {piece[4] (first row / 32, -1 empty), lo/hi of slots 0-1,
+ *                                      lo/hi of slots 2-3 (lo | hi << 6 | lo' << 12 | hi' << 18:
+ *                                      visible rows [lo, hi) of the piece), flags, 0}; flags bit
+ *                                      0 = some slot needs masking, bit 1+k = slot k causal
+ *                                      (mask j > r), bit 5+h = slots 2h, 2h+1 are one 64-row run
+ * flags (entries): bit 0 = causal (mask j > r), bit 1 = the entry does not cover its whole tile. */
 typedef struct {
     int64_t n_rows, n_blocks, n_intervals, n_entries, n_chunks;
     const int32_t *pos_ids;
@@ -166,6 +175,9 @@ typedef struct {
     const int32_t *t_entries;
     const int32_t *chunks;
     const int32_t *fwd_order;
+    int64_t n_ftiles;
+    const int64_t *fblk_ptr;
+    const int32_t *ftiles;
 } ta_plan_arrays;
 
 /* Build the compact prefix-tree episode of a set of token trajectories.

@@ -74,6 +74,8 @@ def check_plan_against_oracle(ep, rows_to_check=None, flags=0, view="mounted"):
             for a, z in want:
                 wmask[a:z] = 1
             assert (mark == wmask).all(), r
+            # the packed tiles of the query-major kernels cover the same rows, once each
+            assert (packed_marks(ex, b, r, N) == wmask).all(), r
     assert (covered == 1).all()
     # causal flag only where some key lies above the block's first row
     for b in range(len(blocks)):
@@ -101,10 +103,52 @@ def check_plan_against_oracle(ep, rows_to_check=None, flags=0, view="mounted"):
     assert (seen == 1).all()
     assert sorted(slots) == list(range(len(slots))) and len(slots) == st["n_partial_slots"]
     assert sorted(ex["fwd_order"].tolist()) == list(range(len(blocks)))
+    check_packed_flags(ex, ep.page_size)
+    fp = ex["fblk_ptr"]
+    assert fp[0] == 0 and (np.diff(fp) >= 1).all() and fp[-1] == len(ex["ftiles"]) == st["n_ftiles"]
+    ntile = np.diff(fp)[ex["fwd_order"]]
+    assert (np.diff(ntile) <= 0).all()       # longest blocks first
     # pair count
     assert st["pairs"] == int((ohi - olo).sum()) == dag.count_pairs(ep.branches, ep.mounts, view=view)
     assert st["n_rows"] == N
     return plan, ex, st
+
+
+def _slots(rec):
+    """(piece, lo, hi, causal) of the 4 slots of a packed tile record."""
+    out = []
+    for k in range(4):
+        w = int(rec[4 + k // 2]) >> (12 * (k % 2))
+        out.append((int(rec[k]), w & 63, (w >> 6) & 63, bool((int(rec[6]) >> (1 + k)) & 1)))
+    return out
+
+
+def packed_marks(ex, b, r, N):
+    """How often each key row is visible to row r through block b's packed tiles."""
+    mark = np.zeros(N + 4 * 32, dtype=np.int32)
+    for rec in ex["ftiles"][ex["fblk_ptr"][b]:ex["fblk_ptr"][b + 1]]:
+        for p, lo, hi, causal in _slots(rec):
+            if p < 0:
+                assert lo == hi == 0
+                continue
+            assert 0 <= lo < hi <= 32
+            a, z = 32 * p + lo, 32 * p + hi
+            if causal:
+                z = min(z, r + 1)
+            mark[a:max(a, z)] += 1
+    assert not mark[N:].any()
+    return mark[:N]
+
+
+def check_packed_flags(ex, page_size):
+    for rec in ex["ftiles"]:
+        sl = _slots(rec)
+        need = any(p < 0 or lo != 0 or hi != 32 or c for p, lo, hi, c in sl)
+        assert bool(rec[6] & 1) == need
+        for h in range(2):
+            if rec[6] & (32 << h):
+                assert page_size >= 64 and rec[2 * h] % 2 == 0 and rec[2 * h + 1] == rec[2 * h] + 1
+        assert rec[7] == 0 and (rec[6] & ~0x7F) == 0
 
 
 def plan_block_rows(ep):
