@@ -634,13 +634,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             for (int u = 0; ok && u < U; ++u) {
                 const int ds = u % kDoStages, qs1 = (u + 1) % kQStages;
+                // Q(u + 1) is checked before P^T(u): dV(u) and S^T(u + 1) then issue back to back
+                if (u + 1 < U && !(ok = mbar_wait(q_full(qs1), ((u + 1) / kQStages) & 1, abort, p.status))) break;
                 if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
                 issue_acc_split(tmem + cDV, tmem + cS, sDO(ds), idesc_o, u > 0);    // dV += P^T dO
                 mma_commit(do_empty(ds));
                 if (u + 1 < U) {
-                    if (!(ok = mbar_wait(q_full(qs1), ((u + 1) / kQStages) & 1, abort, p.status))) break;
-                    tc_fence_after();
                     issue_qk<D>(tmem + cS, sK, sQ(qs1), idesc_s);
                     mma_commit(s_full);
                     mma_commit(q_empty(qs1));
@@ -664,6 +664,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             for (int u = 0; ok && u < U; ++u) {
                 const int qs = u % kQStages, ds1 = (u + 1) % kDoStages;
+                // dO(u + 1) is checked first: dK(u) and dP^T(u + 1) then issue back to back
+                if (u + 1 < U && !(ok = mbar_wait(do_full(ds1), ((u + 1) / kDoStages) & 1, abort, p.status))) break;
                 if (!(ok = mbar_wait(ds_full, u & 1, abort, p.status) &&
                            mbar_wait(s_issued(u), (u >> 1) & 1, abort, p.status)))
                     break;
@@ -671,8 +673,6 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 issue_acc_split(tmem + cDK, tmem + cDP, sQ(qs), idesc_o, u > 0);    // dK += dS^T Q
                 mma_commit(q_empty(qs));
                 if (u + 1 < U) {
-                    if (!(ok = mbar_wait(do_full(ds1), ((u + 1) / kDoStages) & 1, abort, p.status))) break;
-                    tc_fence_after();
                     issue_qk<D>(tmem + cDP, sV, sDO(ds1), idesc_s);
                     mma_commit(dp_full);
                     mma_commit(do_empty(ds1));
