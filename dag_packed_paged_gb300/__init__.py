@@ -11,5 +11,6 @@ from ._native import (  # noqa: F401
     tree_attn_bwd_noalloc,
     tree_attn_bwd_workspace_size, tree_attn_check, tree_attn_fwd, tree_attn_ingest, tree_attn_last_error,
     tree_attn_logprob_bwd, tree_attn_logprob_fwd, tree_attn_logprob_index, tree_attn_owner_mask,
+    tree_attn_place, tree_attn_place_units,
     tree_attn_plan, tree_attn_plan_destroy, tree_attn_plan_export, tree_attn_plan_stats, tree_attn_rope,
     tree_attn_selftest_timeout, tree_attn_set_trace_events)

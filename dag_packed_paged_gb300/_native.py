@@ -70,6 +70,19 @@ class ta_plan_stats(ctypes.Structure):
                 ("device", ctypes.c_int32)]
 
 
+class ta_place_config(ctypes.Structure):
+    _fields_ = [("replicas", ctypes.c_int32), ("mode", ctypes.c_int32), ("capacity", ctypes.c_int64),
+                ("exact_max_traj", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class ta_place_stats(ctypes.Structure):
+    _fields_ = [("total_work", ctypes.c_int64), ("slot_critical_work", ctypes.c_int64),
+                ("max_replica_work", ctypes.c_int64), ("merged_work", ctypes.c_int64),
+                ("n_microbatches", ctypes.c_int32), ("n_slots", ctypes.c_int32), ("n_candidates", ctypes.c_int32),
+                ("source", ctypes.c_int32), ("k_min", ctypes.c_int32), ("k_max", ctypes.c_int32),
+                ("k_natural", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _P32 = ctypes.POINTER(ctypes.c_int32)
 _P64 = ctypes.POINTER(ctypes.c_int64)
 
@@ -137,6 +150,11 @@ def lib():
     L.tree_attn_owner_mask.argtypes = [vp, i32, vp, vp, vp, vp]
     L.tree_attn_owner_mask.restype = ctypes.c_int
     L.tree_attn_ingest.restype = ctypes.c_int
+    L.tree_attn_place.argtypes = [vp, vp, i32, ctypes.POINTER(ta_place_config), vp, vp, vp, vp,
+                                  ctypes.POINTER(ta_place_stats)]
+    L.tree_attn_place.restype = ctypes.c_int
+    L.tree_attn_place_units.argtypes = [vp, i32, i32, vp, vp, ctypes.POINTER(ta_place_stats)]
+    L.tree_attn_place_units.restype = ctypes.c_int
     L.tree_attn_last_error.argtypes = []
     L.tree_attn_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -374,3 +392,43 @@ def tree_attn_logprob_bwd(logits, row_lse, row_ptr, row_pos, pos_target, dlogpro
     C, V = logits.shape
     _check(lib().tree_attn_logprob_bwd(_ptr(logits), C, V, _ptr(row_lse), _ptr(row_ptr), _ptr(row_pos),
                                        _ptr(pos_target), _ptr(dlogprob), _ptr(dlogits), _stream(stream)))
+
+
+def _place_stats(st):
+    return {f: getattr(st, f) for f, _ in ta_place_stats._fields_ if f != "reserved"}
+
+
+def tree_attn_place(trajectories, replicas: int, capacity: int, mode: int = 0, exact_max_traj: int = 0) -> dict:
+    """Compact-work microbatch plan of a list of token trajectories over `replicas` data-parallel
+    replicas (see include/treeattn.h): microbatch of every trajectory, replica / slot / compact
+    rows of every microbatch, and the Eq. 4 objective terms."""
+    trajs = [np.ascontiguousarray(t, dtype=np.int32).ravel() for t in trajectories]
+    n = len(trajs)
+    offsets = np.zeros(n + 1, dtype=np.int64)
+    for i, t in enumerate(trajs):
+        offsets[i + 1] = offsets[i] + len(t)
+    tokens = np.concatenate(trajs) if n and offsets[-1] else np.zeros(1, dtype=np.int32)
+    mb = np.zeros(max(n, 1), dtype=np.int32)
+    rep = np.zeros(max(n, 1), dtype=np.int32)
+    slot = np.zeros(max(n, 1), dtype=np.int32)
+    work = np.zeros(max(n, 1), dtype=np.int64)
+    cfg = ta_place_config(replicas, mode, capacity, exact_max_traj, 0)
+    st = ta_place_stats()
+    _check(lib().tree_attn_place(tokens.ctypes.data, offsets.ctypes.data, n, ctypes.byref(cfg), mb.ctypes.data,
+                                 rep.ctypes.data, slot.ctypes.data, work.ctypes.data, ctypes.byref(st)))
+    K = st.n_microbatches
+    return {"microbatch_of": mb[:n].copy(), "replica_of": rep[:K].copy(), "slot_of": slot[:K].copy(),
+            "work": work[:K].copy(), **_place_stats(st)}
+
+
+def tree_attn_place_units(work, replicas: int) -> dict:
+    """Replica and slot of already-grouped units (e.g. independent DAGs) by the DP-replica
+    assignment of tree_attn_place; work: compact rows (or any additive cost) per unit."""
+    w = np.ascontiguousarray(work, dtype=np.int64)
+    n = len(w)
+    rep = np.zeros(max(n, 1), dtype=np.int32)
+    slot = np.zeros(max(n, 1), dtype=np.int32)
+    st = ta_place_stats()
+    _check(lib().tree_attn_place_units(w.ctypes.data if n else None, n, replicas, rep.ctypes.data,
+                                       slot.ctypes.data, ctypes.byref(st)))
+    return {"replica_of": rep[:n].copy(), "slot_of": slot[:n].copy(), **_place_stats(st)}

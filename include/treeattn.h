@@ -222,6 +222,75 @@ int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, int32_t n_tr
 int tree_attn_owner_mask(const int64_t *offsets, int32_t n_traj, const int64_t *row_of,
                          const int32_t *row_owner, const uint8_t *generated, uint8_t *mask);
 
+/* Compact-work microbatch planning across data-parallel replicas (HARTS, arXiv 2608.28158,
+ * Section 3.2).  Complete trajectories (the smallest scheduling unit) are grouped into K
+ * microbatches of at most `capacity` compact rows each -- a microbatch's work is the row count of
+ * the compact trie of its trajectories (Eq. 5) -- with K a multiple of `replicas` (D), and each
+ * microbatch is given a replica and a slot.  Plans are ranked lexicographically by Eq. 4: total
+ * compact work, then the sum over slots of the slot's heaviest microbatch, then the heaviest
+ * replica's cumulative work.  Candidate groupings (mode 0 uses both kinds, 1 only the first, 2
+ * only the second):
+ *   - partitions contiguous in lexicographic order for every K of Eq. 8, K from K_min of Eq. 7
+ *     (D max(1, ceil(G / (T D))), G the work of all trajectories in one trie) to K_max (from the
+ *     natural partition, which splits every interval heavier than T at its lowest adjacent-LCP
+ *     valley): the exact dynamic program of Eq. 9 for up to `exact_max_traj` trajectories (0:
+ *     512), else the natural partition evolved by merging the adjacent pair that saves the most
+ *     and splitting at the lowest valley, over at most 32 sampled K;
+ *   - greedy insertion by the exact compact-work increase of Eq. 10, in four processing orders
+ *     (ascending and descending lexicographic, descending length, descending unique-suffix score)
+ *     under two policies (best fit: the largest work after insertion; max shared: the largest
+ *     |x| - increase), K raised to a multiple of D by splitting off the single trajectories that
+ *     cost the least; of the eight, the one with the fewest microbatches, then the least work.
+ * Every candidate gets the DP-replica assignment of the section: microbatches sorted by work,
+ * each consecutive block of D one slot, the heavier ones to the replicas with less work so far.
+ * Not built (they refine a candidate without changing what the planner guarantees): boundary
+ * refinement and sparse repair.
+ *
+ *   tokens, offsets, n_traj   host: trajectory i is tokens[offsets[i] .. offsets[i+1]),
+ *                             non-empty, no longer than capacity; n_traj >= replicas
+ *   microbatch_of             host, out, int32[n_traj]: microbatch of each trajectory
+ *   replica_of, slot_of       host, out, int32[n_traj] (capacity; the first K are written):
+ *                             replica and slot of each microbatch; every replica gets exactly
+ *                             one microbatch per slot
+ *   mb_work                   host, out, int64[n_traj] or NULL: compact rows of each microbatch
+ * Returns TA_OK, or TA_ERR_INVALID (arguments, a trajectory longer than the capacity, no
+ * feasible plan), TA_ERR_NOMEM.  Pure host code. */
+typedef struct {
+    int32_t replicas;        /* D >= 1 */
+    int32_t mode;            /* 0: contiguous and greedy candidates; 1: contiguous only; 2: greedy only */
+    int64_t capacity;        /* T: compact rows per microbatch at most */
+    int32_t exact_max_traj;  /* exact dynamic program up to this many trajectories (0: 512) */
+    int32_t reserved;
+} ta_place_config;
+
+typedef struct {
+    int64_t total_work;          /* Eq. 4, first term: sum of the microbatches' compact rows */
+    int64_t slot_critical_work;  /* Eq. 4, second term: sum over slots of the heaviest microbatch */
+    int64_t max_replica_work;    /* Eq. 4, third term: the heaviest replica's cumulative work */
+    int64_t merged_work;         /* G: compact rows of all trajectories in one trie */
+    int32_t n_microbatches;      /* K */
+    int32_t n_slots;             /* K / D */
+    int32_t n_candidates;        /* candidate plans compared */
+    int32_t source;              /* the chosen plan's generator: 0 contiguous, 1 greedy */
+    int32_t k_min, k_max;        /* Eq. 7-8 */
+    int32_t k_natural;           /* microbatches of the natural partition */
+    int32_t reserved;
+} ta_place_stats;
+
+int tree_attn_place(const int32_t *tokens, const int64_t *offsets, int32_t n_traj, const ta_place_config *cfg,
+                    int32_t *microbatch_of, int32_t *replica_of, int32_t *slot_of, int64_t *mb_work,
+                    ta_place_stats *stats);
+
+/* The DP-replica assignment of tree_attn_place for units that are already grouped -- e.g. the
+ * independent DAGs of a batch of episodes, whose attention shares no rows across units, so that
+ * each replica runs its units with no collective: units sorted by work, each consecutive block of
+ * `replicas` one slot (the last one may be short), the heavier units of a slot to the replicas
+ * with less work so far.  work: host int64[n_units] (compact rows, or any additive cost);
+ * replica_of, slot_of: host out int32[n_units]; stats as tree_attn_place (n_microbatches =
+ * n_units).  Returns TA_OK or TA_ERR_INVALID. */
+int tree_attn_place_units(const int64_t *work, int32_t n_units, int32_t replicas, int32_t *replica_of,
+                          int32_t *slot_of, ta_place_stats *stats);
+
 /*
  * tree_attn_plan -- validate an episode DAG and build the work plan (host C++).
  *
