@@ -152,6 +152,32 @@ def rank_seed(seed: int, rank: int) -> int:
     return seed + rank
 
 
+def rank_episode(make, world: int, rank: int):
+    """The rank's share of a global batch of `world` episodes (seeds 0 .. world-1) of one shape:
+    the batch's independent DAGs (no row of one is visible to another, so no collective is
+    needed in the attention) are placed on the ranks by the replica assignment of HARTS Section
+    3.2 on their compact rows, and the rank's DAGs are packed into one strip, in batch order.
+    Weak scaling: each rank gets one episode's worth of DAGs.  With one rank the strip is the
+    episode itself.  Returns the rank's episode, the placement summary and the indices (in the
+    global batch) of the rank's DAGs."""
+    import dag_packed_paged_gb300 as ta
+    units = []
+    for s in range(world):
+        ep = make()
+        ep.seed = s
+        units += W.split_dags(ep)
+    work = np.array([u.n_rows for u in units], dtype=np.int64)
+    pl = ta.tree_attn_place_units(work, world)
+    mine = [u for u, r in zip(units, pl["replica_of"]) if r == rank]
+    loads = np.bincount(pl["replica_of"], weights=work, minlength=world)
+    ep = W.concat_episodes(mine, name=units[0].name.split("/dag")[0], seed=rank_seed(0, rank))
+    info = {"dags": len(units), "dags_per_rank": np.bincount(pl["replica_of"], minlength=world).tolist(),
+            "max_rank_rows": int(pl["max_replica_work"]), "imbalance": float(loads.max() / loads.mean()),
+            "placement": "independent DAGs of the global batch on ranks by the replica assignment of "
+                         "HARTS Section 3.2 (compact rows); no collective in the attention"}
+    return ep, info, [i for i, r in enumerate(pl["replica_of"]) if r == rank]
+
+
 def bf16_dev(bits, dev):
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -433,6 +459,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     ep = W.config(WORKLOADS[args.workload])
+    placement = None
 
     if args.impl == "reference":
         run_reference(args, ep, world, rank)
@@ -452,7 +479,7 @@ def main():
     torch.cuda.set_device(dev)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    ep.seed = rank_seed(ep.seed, rank)
+    ep, placement, _ = rank_episode(lambda: W.config(WORKLOADS[args.workload]), world, rank)
     t = W.make_tensors(ep)
     pool = W.make_pool(ep, t)
     N, Hq, Hkv, D = ep.n_rows, ep.num_q_heads, ep.num_kv_heads, ep.head_dim
@@ -617,7 +644,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(ep, args, st),
+        "data": "synthetic", "config": dict(workload_config(ep, args, st), sharding=placement),
         "fwd_tflops": fwd_tflops,
         "fwd_frac_of_peak": fwd_tflops / burst, "fwdbwd_frac_of_peak": value / world / burst,
         "fwd_frac_of_nominal": fwd_tflops / NOMINAL_BF16_TFLOPS,

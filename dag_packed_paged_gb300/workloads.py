@@ -377,6 +377,73 @@ def random_small(seed: int, max_branches: int = 7, max_len: int = 160, heads=(4,
 
 
 # --------------------------------------------------------------------------------------
+# independent DAGs of an episode (for placing them on data-parallel replicas)
+# --------------------------------------------------------------------------------------
+
+def split_dags(ep: Episode) -> list[Episode]:
+    """The episode's connected components under fork and mount edges: DAGs that share no rows,
+    so that their attention is independent.  Each keeps its branches in index order and its
+    rows in strip order (row_start compacted), with the episode's attention shape."""
+    br, mt = ep.branches, ep.mounts
+    nb = len(br)
+    up = list(range(nb))
+
+    def find(x):
+        while up[x] != x:
+            up[x] = up[up[x]]
+            x = up[x]
+        return x
+
+    for b in range(nb):
+        p = int(br["parent"][b])
+        if p >= 0:
+            up[find(b)] = find(p)
+    for m in mt:
+        up[find(int(m["reader"]))] = find(int(m["source"]))
+    comps = {}
+    for b in range(nb):
+        comps.setdefault(find(b), []).append(b)
+    out = []
+    for members in sorted(comps.values(), key=lambda ms: int(br["row_start"][ms[0]])):
+        idx = {b: i for i, b in enumerate(members)}
+        sub = br[members].copy()
+        sub["parent"] = [idx[int(p)] if p >= 0 else -1 for p in sub["parent"]]
+        order = np.argsort(sub["row_start"], kind="stable")
+        start, cur = np.zeros(len(sub), np.int64), 0
+        for i in order:
+            start[i] = cur
+            cur += int(sub["length"][i])
+        sub["row_start"] = start
+        rows = [tuple(int(x) for x in m) for m in mt if int(m["reader"]) in idx]
+        sm = make_mounts([(idx[r], t, idx[s], b0, e) for (r, t, s, b0, e) in rows])
+        out.append(Episode(f"{ep.name}/dag{len(out)}", sub, sm, ep.num_q_heads, ep.num_kv_heads, ep.head_dim,
+                           ep.page_size, ep.seed))
+    return out
+
+
+def concat_episodes(eps: list[Episode], name: str = "batch", seed: int = 0) -> Episode:
+    """One strip holding the given episodes one after another (branch and mount indices and
+    row starts shifted); they must share the attention shape."""
+    e0 = eps[0]
+    brs, mts, nb, rows = [], [], 0, 0
+    for ep in eps:
+        assert (ep.num_q_heads, ep.num_kv_heads, ep.head_dim, ep.page_size) == \
+            (e0.num_q_heads, e0.num_kv_heads, e0.head_dim, e0.page_size)
+        b = ep.branches.copy()
+        b["parent"] = np.where(b["parent"] >= 0, b["parent"] + nb, -1)
+        b["row_start"] += rows
+        brs.append(b)
+        m = ep.mounts.copy()
+        m["reader"] += nb
+        m["source"] += nb
+        mts.append(m)
+        nb += len(b)
+        rows += ep.n_rows
+    return Episode(name, np.concatenate(brs), np.concatenate(mts).astype(MOUNT_DTYPE), e0.num_q_heads,
+                   e0.num_kv_heads, e0.head_dim, e0.page_size, seed)
+
+
+# --------------------------------------------------------------------------------------
 # tensors and pool
 # --------------------------------------------------------------------------------------
 
