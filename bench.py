@@ -254,7 +254,10 @@ def run_reference(args, ep, world, rank):
 
 
 def workload_config(ep, args, stats=None):
-    cfg = {"workload": DESCRIPTION[WORKLOADS[args.workload]], "name": args.workload, "rows": ep.n_rows,
+    desc = DESCRIPTION[WORKLOADS[args.workload]]
+    if getattr(args, "scale", 1) != 1:
+        desc = f"{desc} -- every length divided by {args.scale} (profiling case)"
+    cfg = {"workload": desc, "name": args.workload, "rows": ep.n_rows,
            "branches": int(len(ep.branches)), "mounts": int(len(ep.mounts)),
            "heads_q": ep.num_q_heads, "heads_kv": ep.num_kv_heads, "head_dim": ep.head_dim,
            "page_size": ep.page_size, "seed": ep.seed}
@@ -446,6 +449,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clock-log", default=None, help="keep the raw nvidia-smi clock samples in this CSV file")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="divide every length of the workload by this factor (a small case of the same shape, for "
+                         "profiler captures; not a benchmark line)")
     ap.add_argument("--also", default="commander_worker_dag,irregular_tree",
                     help="comma-separated workloads also timed (device-resident fwd + bwd) at N = 1 and "
                          "reported under other_workloads; empty for none")
@@ -479,7 +485,9 @@ def main():
     torch.cuda.set_device(dev)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    ep, placement, _ = rank_episode(lambda: W.config(WORKLOADS[args.workload]), world, rank)
+    make = (lambda: W.config(WORKLOADS[args.workload])) if args.scale == 1 else \
+        (lambda: W.scaled(WORKLOADS[args.workload], args.scale))
+    ep, placement, _ = rank_episode(make, world, rank)
     t = W.make_tensors(ep)
     pool = W.make_pool(ep, t)
     N, Hq, Hkv, D = ep.n_rows, ep.num_q_heads, ep.num_kv_heads, ep.head_dim

@@ -57,62 +57,90 @@ int fail(int code, const std::string &msg) {
 // forms a 64-row half (one TMA box when pages hold >= 64 rows), the other pieces pair up into
 // halves of two single boxes; halves fill tiles in order.  Rows outside the block's visible
 // set occupy only the uncovered ends of pieces and the empty slot of a last half or tile.
-void pack_block_tiles(const std::vector<std::pair<Interval, bool>> &items, int64_t r0, bool half_boxes,
-                      std::vector<int32_t> &out) {
-    struct Piece {
-        int64_t q;
-        int32_t lo, hi;
-        bool causal;
-    };
-    std::vector<Piece> pcs;
-    for (const auto &it : items) {
-        const Interval x = it.first;
-        for (int64_t q = x.lo / kPieceRows; q * kPieceRows < x.hi; ++q) {
-            const int64_t a = std::max<int64_t>(x.lo, q * kPieceRows), z = std::min<int64_t>(x.hi, (q + 1) * kPieceRows);
-            pcs.push_back({q, int32_t(a - q * kPieceRows), int32_t(z - q * kPieceRows), it.second && z - 1 > r0});
-        }
-    }
-    std::stable_sort(pcs.begin(), pcs.end(), [](const Piece &a, const Piece &b) {
-        return a.q < b.q || (a.q == b.q && a.lo < b.lo);
-    });
-    const Piece none{-1, 0, 0, false};
-    std::vector<std::array<Piece, 2>> halves;
-    std::vector<bool> joined;                 // the half is one 64-row-aligned run
-    const Piece *single = nullptr;
-    for (size_t i = 0; i < pcs.size(); ++i) {
-        if (pcs[i].q % 2 == 0 && i + 1 < pcs.size() && pcs[i + 1].q == pcs[i].q + 1) {
-            halves.push_back({pcs[i], pcs[i + 1]});
-            joined.push_back(half_boxes);
-            ++i;
-        } else if (single) {
-            halves.push_back({*single, pcs[i]});
-            joined.push_back(false);
-            single = nullptr;
-        } else {
-            single = &pcs[i];
-        }
-    }
-    if (single) {
-        halves.push_back({*single, none});
-        joined.push_back(false);
-    }
-    for (size_t h = 0; h < halves.size(); h += 2) {
-        Piece s[4] = {halves[h][0], halves[h][1], none, none};
-        int32_t flags = joined[h] ? kPackHalf64 : 0;
-        if (h + 1 < halves.size()) {
-            s[2] = halves[h + 1][0];
-            s[3] = halves[h + 1][1];
-            if (joined[h + 1]) flags |= kPackHalf64 << 1;
-        }
+// Streams the pieces (no per-block allocation: the planner calls this once per block).
+struct Piece {
+    int64_t q;
+    int32_t lo, hi;
+    bool causal;
+};
+
+struct Packer {
+    std::vector<std::pair<Interval, bool>> its;
+    Piece half[2][2];
+    bool joined[2];
+    int n_halves = 0;
+    Piece single{-1, 0, 0, false}, even{-1, 0, 0, false};
+    bool have_single = false, have_even = false, half_boxes = false;
+    std::vector<int32_t> *out = nullptr;
+
+    void emit_tile() {
+        const Piece none{-1, 0, 0, false};
+        Piece s[4] = {half[0][0], half[0][1], n_halves > 1 ? half[1][0] : none, n_halves > 1 ? half[1][1] : none};
+        int32_t flags = (joined[0] ? kPackHalf64 : 0) | (n_halves > 1 && joined[1] ? kPackHalf64 << 1 : 0);
         for (int k = 0; k < 4; ++k) {
             if (s[k].causal) flags |= kPackCausal << k;
             if (s[k].q < 0 || s[k].lo != 0 || s[k].hi != kPieceRows || s[k].causal) flags |= kPackMask;
         }
-        out.insert(out.end(), {int32_t(s[0].q), int32_t(s[1].q), int32_t(s[2].q), int32_t(s[3].q),
-                               s[0].lo | s[0].hi << 6 | s[1].lo << 12 | s[1].hi << 18,
-                               s[2].lo | s[2].hi << 6 | s[3].lo << 12 | s[3].hi << 18, flags, 0});
+        const int32_t rec[kPackInts] = {int32_t(s[0].q), int32_t(s[1].q), int32_t(s[2].q), int32_t(s[3].q),
+                                        s[0].lo | s[0].hi << 6 | s[1].lo << 12 | s[1].hi << 18,
+                                        s[2].lo | s[2].hi << 6 | s[3].lo << 12 | s[3].hi << 18, flags, 0};
+        out->insert(out->end(), rec, rec + kPackInts);
+        n_halves = 0;
     }
-}
+    void push_half(const Piece &a, const Piece &b, bool j) {
+        half[n_halves][0] = a;
+        half[n_halves][1] = b;
+        joined[n_halves] = j;
+        if (++n_halves == 2) emit_tile();
+    }
+    void push_single(const Piece &p) {
+        if (have_single) {
+            push_half(single, p, false);
+            have_single = false;
+        } else {
+            single = p;
+            have_single = true;
+        }
+    }
+    // pieces arrive in (q, lo) order; an even piece waits to see whether the next one is q + 1
+    void add(const Piece &p) {
+        if (have_even) {
+            have_even = false;
+            if (p.q == even.q + 1) {
+                push_half(even, p, half_boxes);
+                return;
+            }
+            push_single(even);
+        }
+        if (p.q % 2 == 0) {
+            even = p;
+            have_even = true;
+        } else {
+            push_single(p);
+        }
+    }
+
+    void run(const std::vector<std::pair<Interval, bool>> &items, int64_t r0, bool hb, std::vector<int32_t> &dst) {
+        out = &dst;
+        half_boxes = hb;
+        its.assign(items.begin(), items.end());
+        std::sort(its.begin(), its.end(), [](const std::pair<Interval, bool> &a, const std::pair<Interval, bool> &b) {
+            return a.first.lo < b.first.lo;
+        });
+        n_halves = 0;
+        have_single = have_even = false;
+        for (const auto &it : its) {
+            const Interval x = it.first;
+            for (int64_t q = x.lo / kPieceRows; q * kPieceRows < x.hi; ++q) {
+                const int64_t a = std::max<int64_t>(x.lo, q * kPieceRows), z = std::min<int64_t>(x.hi, (q + 1) * kPieceRows);
+                add({q, int32_t(a - q * kPieceRows), int32_t(z - q * kPieceRows), it.second && z - 1 > r0});
+            }
+        }
+        if (have_even) push_single(even);
+        if (have_single) push_half(single, Piece{-1, 0, 0, false}, false);
+        if (n_halves == 1) emit_tile();
+    }
+};
 
 }  // namespace
 
@@ -421,6 +449,8 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
 
     // ------------------------------------------------------------------ key-tile entries
     P.fblk_ptr.assign(1, 0);
+    Packer packer;
+    P.ftiles.reserve(size_t(n_blocks) * 64 * kPackInts);
     for (int64_t qb = 0; qb < n_blocks; ++qb) {
         const int64_t r0 = blocks[4 * qb];
         blocks[4 * qb + 2] = (int32_t)(P.entries.size() / 4);
@@ -446,7 +476,7 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
             }
         }
         blocks[4 * qb + 3] = (int32_t)(P.entries.size() / 4);
-        pack_block_tiles(items, r0, Pg >= 64, P.ftiles);
+        packer.run(items, r0, Pg >= 64, P.ftiles);
         P.fblk_ptr.push_back((int64_t)(P.ftiles.size() / kPackInts));
     }
     const int64_t n_entries = (int64_t)P.entries.size() / 4;
