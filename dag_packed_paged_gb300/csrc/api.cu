@@ -117,22 +117,35 @@ int make_maps(const ta_plan *plan, const void *q, const void *k_pool, const void
 // Stream-ordered plan upload (TA_PLAN_STREAM_ORDERED).  A copy from pageable memory is staged
 // by the driver in chunks whose DMA is queued on the copy's stream, so on a stream still busy
 // with earlier kernels the call blocks the host until they finish.  The upload therefore runs
-// on an internal stream that nothing else uses, from a pinned staging buffer reused across
-// plans, and the caller's stream waits for it through an event: the host never waits for the
-// caller's earlier work.
-struct Uploader {
-    std::mutex mu;
-    cudaStream_t stream = nullptr;
+// on an internal stream that nothing else uses, from pinned staging buffers, and the caller's
+// stream waits for it through an event: the host never waits for the caller's earlier work.
+// The staging buffers form a ring of kUploadSlots, each with the event of its last copy: a
+// copy engine busy with the caller's own large transfers delays a plan's upload, and with a
+// single buffer the next plan would wait on the host for it.
+constexpr int kUploadSlots = 4;
+struct UploadSlot {
     cudaEvent_t done = nullptr;   // recorded after the last copy out of `pinned`
     void *pinned = nullptr;
     size_t cap = 0;
 };
+struct Uploader {
+    std::mutex mu;
+    cudaStream_t stream = nullptr;
+    UploadSlot slot[kUploadSlots];
+    int next = 0;
+};
 constexpr int kMaxUploadDevices = 64;
 Uploader g_uploader[kMaxUploadDevices];
 
-// Allocates *dst (stream-ordered) and copies `bytes` from host `src` into it; work enqueued on
-// `user` after this call is ordered after the copy.
-int upload_stream_ordered(int dev, void **dst, const void *src, size_t bytes, cudaStream_t user) {
+struct Part {
+    const void *src;
+    size_t bytes;
+    size_t off;
+};
+
+// Allocates *dst (stream-ordered) and fills it with `parts` (each at its offset, `total` bytes in
+// all); work enqueued on `user` after this call is ordered after the copy.
+int upload_stream_ordered(int dev, void **dst, const Part *parts, int n_parts, size_t total, cudaStream_t user) {
     if (dev < 0 || dev >= kMaxUploadDevices) {
         set_error("device index beyond the supported range");
         return TA_ERR_UNSUPPORTED;
@@ -141,19 +154,25 @@ int upload_stream_ordered(int dev, void **dst, const void *src, size_t bytes, cu
     std::lock_guard<std::mutex> lock(u.mu);
     cudaError_t e = cudaSuccess;
     if (!u.stream) e = cudaStreamCreateWithFlags(&u.stream, cudaStreamNonBlocking);
-    if (e == cudaSuccess && !u.done) e = cudaEventCreateWithFlags(&u.done, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventSynchronize(u.done);   // the previous copy has left `pinned`
-    if (e == cudaSuccess && u.cap < bytes) {
-        if (u.pinned) cudaFreeHost(u.pinned);
-        u.pinned = nullptr;
-        u.cap = 0;
-        e = cudaMallocHost(&u.pinned, bytes);
-        if (e == cudaSuccess) u.cap = bytes;
+    UploadSlot &sl = u.slot[u.next];
+    u.next = (u.next + 1) % kUploadSlots;
+    if (e == cudaSuccess && !sl.done) e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventSynchronize(sl.done);   // this slot's previous copy has left it
+    if (e == cudaSuccess && sl.cap < total) {
+        if (sl.pinned) cudaFreeHost(sl.pinned);
+        sl.pinned = nullptr;
+        sl.cap = 0;
+        e = cudaMallocHost(&sl.pinned, total);
+        if (e == cudaSuccess) sl.cap = total;
     }
     if (e != cudaSuccess) return cuda_fail(e, "plan upload (staging)");
-    std::memcpy(u.pinned, src, bytes);
+    uint8_t *stage = static_cast<uint8_t *>(sl.pinned);
+    for (int i = 0; i < n_parts; ++i) {   // a part without a source (the status words) starts zeroed
+        if (parts[i].src && parts[i].bytes) std::memcpy(stage + parts[i].off, parts[i].src, parts[i].bytes);
+        else if (!parts[i].src) std::memset(stage + parts[i].off, 0, parts[i].bytes);
+    }
     *dst = nullptr;
-    e = cudaMallocAsync(dst, bytes, u.stream);
+    e = cudaMallocAsync(dst, total, u.stream);
     if (e != cudaSuccess) {
         *dst = nullptr;
         if (e == cudaErrorMemoryAllocation) {
@@ -162,9 +181,9 @@ int upload_stream_ordered(int dev, void **dst, const void *src, size_t bytes, cu
         }
         return cuda_fail(e, "plan upload (allocation)");
     }
-    e = cudaMemcpyAsync(*dst, u.pinned, bytes, cudaMemcpyHostToDevice, u.stream);
-    if (e == cudaSuccess) e = cudaEventRecord(u.done, u.stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, u.done, 0);
+    e = cudaMemcpyAsync(*dst, stage, total, cudaMemcpyHostToDevice, u.stream);
+    if (e == cudaSuccess) e = cudaEventRecord(sl.done, u.stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, sl.done, 0);
     if (e != cudaSuccess) {
         cudaFreeAsync(*dst, u.stream);
         *dst = nullptr;
@@ -230,11 +249,6 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     }
 
     // one device buffer for every array the kernels read, plus status words
-    struct Part {
-        const void *src;
-        size_t bytes;
-        size_t off;
-    };
     std::vector<int32_t> fblk(2 * (h.fblk_ptr.size() - 1));
     for (size_t b = 0; b + 1 < h.fblk_ptr.size(); ++b) {
         fblk[2 * b] = int32_t(h.fblk_ptr[b]);
@@ -254,19 +268,19 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         p.off = total;
         total = align_up(total + std::max<size_t>(p.bytes, 16), 256);
     }
-    std::vector<uint8_t> staging(total, 0);
-    for (Part &p : parts)
-        if (p.src && p.bytes) std::memcpy(staging.data() + p.off, p.src, p.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     plan->stream_ordered = (h.cfg.flags & TA_PLAN_STREAM_ORDERED) != 0;
     plan->stream = stream;
     cudaError_t e = cudaSuccess;
     if (plan->stream_ordered) {
-        if ((rc = upload_stream_ordered(plan->device, &plan->d_buf, staging.data(), total, s))) {
+        if ((rc = upload_stream_ordered(plan->device, &plan->d_buf, parts, 13, total, s))) {
             delete plan;
             return rc;
         }
     } else {
+        std::vector<uint8_t> staging(total, 0);
+        for (Part &p : parts)
+            if (p.src && p.bytes) std::memcpy(staging.data() + p.off, p.src, p.bytes);
         e = cudaMalloc(&plan->d_buf, total);
         if (e != cudaSuccess) {
             delete plan;
