@@ -215,15 +215,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_ready, 256);
+        mbar_init(q_ready, 8);                // one arrival per elementwise warp
         mbar_init(do_full, 1);
         for (int s = 0; s < kKStages; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
         mbar_init(s_full, 1);
-        mbar_init(s_free, 256);
+        mbar_init(s_free, 8);
         mbar_init(dp_full, 1);
-        mbar_init(dp_free, 256);
-        mbar_init(ds_full, 256);
+        mbar_init(dp_free, 8);
+        mbar_init(ds_full, 8);
         mbar_init(ds_free, 1);
         mbar_init(o_full, 2);                 // one commit from each MMA issuer
         *abort = 0;
@@ -356,7 +356,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         row_to_tmem<D>(tmem + lane_off + cQ, p.q + (static_cast<size_t>(r_abs) * p.Hq + h) * D, valid, w);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(q_ready);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
         const float sl2 = p.scale_log2;
         const float *tab = p.utab + (static_cast<size_t>(g * p.n_blocks + qb) * 2 + t) * 256;
         const float nlse2 = tab[32 * q4 + lane];      // -lse * log2(e)
@@ -377,7 +378,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_ld32(tmem + lane_off + cS + 64 * w + 32, sv[1]);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(s_free);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
                 const uint64_t sc2 = f2_pack(sl2, sl2), nl2 = f2_pack(nlse2, nlse2);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -410,7 +412,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_ld32(tmem + lane_off + cDP + 64 * w + 32, dpv[1]);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(dp_free);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dp_free);
                 uint32_t ds[2][16];
                 const uint64_t nd2 = f2_pack(ndelta, ndelta);
 #pragma unroll
@@ -431,7 +434,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 tmem_st16(tmem + lane_off + cDS + 32 * w + 16, ds[1]);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(ds_full);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_full);
             }
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
@@ -552,8 +556,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         for (int s = 0; s < kDoStages; ++s) { mbar_init(do_full(s), 1); mbar_init(do_empty(s), 2); }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_full, 256);
-        mbar_init(ds_full, 256);
+        mbar_init(p_full, 8);                 // one arrival per elementwise warp
+        mbar_init(ds_full, 8);
         mbar_init(o_full, 2);
         *abort = 0;
         fence_barrier_init();
@@ -742,7 +746,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tmem_st16(tmem + lane_off + cS + 64 * w + 16, pk[1]);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(p_full);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
             }
             // ---------------- phase 2: dS^T
             ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, abort, p.status) &&
@@ -772,7 +777,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tmem_st16(tmem + lane_off + cDP + 64 * w + 16, dk[1]);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(ds_full);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_full);
             }
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
