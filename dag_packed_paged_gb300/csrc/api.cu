@@ -204,6 +204,7 @@ const char *tree_attn_last_error(void) { return g_last_error.c_str(); }
 int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount *mounts, int32_t n_mounts,
                    const int32_t *page_table, int64_t n_logical_pages, const ta_config *config,
                    int32_t *pos_ids_out, void *stream, ta_plan **out) {
+    NvtxRange nvtx_range("tree_attn_plan");
     if (!out) {
         set_error("out is NULL");
         return TA_ERR_INVALID;
@@ -412,6 +413,7 @@ static int check_device(const ta_plan *plan, const char *who) {
 }
 
 int tree_attn_check(const ta_plan *plan, void *stream) {
+    NvtxRange nvtx_range("tree_attn_check");
     if (!plan) {
         set_error("plan is NULL");
         return TA_ERR_INVALID;
@@ -443,6 +445,7 @@ int tree_attn_check(const ta_plan *plan, void *stream) {
 
 int tree_attn_logprob_fwd(const void *logits, int64_t n_rows, int64_t vocab, const int64_t *pos_row,
                           const int32_t *pos_target, int64_t n_pos, float *row_lse, float *logprob, void *stream) {
+    NvtxRange nvtx_range("tree_attn_logprob_fwd");
     if (n_rows < 0 || n_pos < 0 || vocab <= 0 || vocab > INT32_MAX) {
         set_error("tree_attn_logprob_fwd: bad sizes");
         return TA_ERR_INVALID;
@@ -463,6 +466,7 @@ int tree_attn_logprob_fwd(const void *logits, int64_t n_rows, int64_t vocab, con
 int tree_attn_logprob_bwd(const void *logits, int64_t n_rows, int64_t vocab, const float *row_lse,
                           const int64_t *row_ptr, const int64_t *row_pos, const int32_t *pos_target,
                           const float *dlogprob, void *dlogits, void *stream) {
+    NvtxRange nvtx_range("tree_attn_logprob_bwd");
     if (n_rows < 0 || vocab <= 0 || vocab > INT32_MAX) {
         set_error("tree_attn_logprob_bwd: bad sizes");
         return TA_ERR_INVALID;
@@ -483,6 +487,7 @@ int tree_attn_logprob_bwd(const void *logits, int64_t n_rows, int64_t vocab, con
 }
 
 int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base, void *stream) {
+    NvtxRange nvtx_range("tree_attn_rope");
     if (!plan) {
         set_error("plan is NULL");
         return TA_ERR_INVALID;
@@ -516,6 +521,7 @@ int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base
 
 int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool, void *o,
                   float *lse, void *stream) {
+    NvtxRange nvtx_range("tree_attn_fwd");
     if (!plan) {
         set_error("plan is NULL");
         return TA_ERR_INVALID;
@@ -560,6 +566,7 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
 int tree_attn_bwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool, const void *o,
                   const float *lse, const void *d_o, float *dq, float *dk_pool, float *dv_pool, void *workspace,
                   size_t ws_bytes, void *stream) {
+    NvtxRange nvtx_range("tree_attn_bwd");
     if (!plan) {
         set_error("plan is NULL");
         return TA_ERR_INVALID;

@@ -120,6 +120,18 @@ __device__ __forceinline__ void issue_acc_split(uint32_t d_tmem, uint32_t a_base
                b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc, (acc || kk > 0) ? 1u : 0u);
 }
 
+// Half h of issue_acc_split: the K-columns [64w + 32h, 64w + 32h + 32) of both groups w.
+__device__ __forceinline__ void issue_acc_half(uint32_t d_tmem, uint32_t a_base, uint32_t sB, uint32_t idesc, int h,
+                                               bool acc) {
+    const uint64_t b0 = sdesc_sw128(sB, kTileRows * 128, 1024);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int kk = 4 * (i >> 1) + 2 * h + (i & 1);
+        mma_ts(d_tmem, a_base + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+               b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc, (acc || i > 0) ? 1u : 0u);
+    }
+}
+
 // D[128 x N] (+)= A[128 x 128] * B[128 x N], A in bf16 TMEM columns [a_base, a_base + 64)
 // (K-column k in column a_base + k / 2), B the rows of an MN-major smem tile.
 __device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_base, uint32_t sB, uint32_t idesc, bool acc) {
@@ -480,7 +492,7 @@ struct DkvLayout {
     static constexpr int lse_off = do_off + kDoStages * kTile;     // per dO stage: 128 floats
     static constexpr int dl_off = lse_off + kDoStages * 512;       // per Q stage: 128 floats
     static constexpr int bar_off = dl_off + kQStages * 512;
-    static constexpr int n_bars = 1 + 2 * kQStages + 2 * kDoStages + 7;
+    static constexpr int n_bars = 1 + 2 * kQStages + 2 * kDoStages + 8;
     static constexpr int misc_off = bar_off + n_bars * 8;
     static constexpr int bytes = misc_off + 16;                     // the base is 1024-aligned
 };
@@ -489,8 +501,10 @@ struct DkvLayout {
 // shared memory.  Every (reader block, 128-lane query tile) is one unit, processed in two
 // phases so that the tensor core always has work while the elementwise warps run:
 //   MMA:  S^T = K Q^T, dP^T = V dO^T                       (128 x 128 each, into TMEM)
-//   EW :  P^T = exp2(S^T log2e scale - lse) (masked), bf16 copy into TMEM      -> p_full
-//   MMA:  dV += P^T dO,  then the next unit's S^T             (while EW computes dS)
+//   EW :  P^T = exp2(S^T log2e scale - lse) (masked), bf16 copy into TMEM, in two halves of
+//         each group's columns                                     -> p_full, p_half1
+//   MMA:  dV += P^T dO (the first halves' K-steps while EW exponentiates the second halves),
+//         then the next unit's S^T                                 (while EW computes dS)
 //   EW :  dS^T = P^T (dP^T - delta), bf16 copy into TMEM                        -> ds_full
 //   MMA:  dK += dS^T Q,  then the next unit's dP^T            (while EW computes the next P)
 // The two elementwise warpgroups split each unit's 128 query columns (64 each); P stays in
@@ -545,6 +559,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t o_full = bar(kb + 4);
     // S^T(u + 1) has been issued (two barriers, alternating by unit): the dK issuer waits for it
     auto s_issued = [&](int u) { return bar(kb + 5 + (u & 1)); };
+    const uint32_t p_half1 = bar(kb + 7);   // second half of each group's P^T columns
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
 
@@ -557,6 +572,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
         mbar_init(p_full, 8);                 // one arrival per elementwise warp
+        mbar_init(p_half1, 8);
         mbar_init(ds_full, 8);
         mbar_init(o_full, 2);
         *abort = 0;
@@ -642,7 +658,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (u + 1 < U && !(ok = mbar_wait(q_full(qs1), ((u + 1) / kQStages) & 1, abort, p.status))) break;
                 if (!(ok = mbar_wait(p_full, u & 1, abort, p.status))) break;
                 tc_fence_after();
-                issue_acc_split(tmem + cDV, tmem + cS, sDO(ds), idesc_o, u > 0);    // dV += P^T dO
+                issue_acc_half(tmem + cDV, tmem + cS, sDO(ds), idesc_o, 0, u > 0);  // dV += P^T dO, first halves
+                if (!(ok = mbar_wait(p_half1, u & 1, abort, p.status))) break;
+                tc_fence_after();
+                issue_acc_half(tmem + cDV, tmem + cS, sDO(ds), idesc_o, 1, true);   // second halves
                 mma_commit(do_empty(ds));
                 if (u + 1 < U) {
                     issue_qk<D>(tmem + cS, sK, sQ(qs1), idesc_s);
@@ -709,45 +728,48 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const bool causal = (te.x & kEntryCausal) != 0;
             // query row of lane m of this group's columns: first row + ((128 t + 64 w + m) mod R)
             const int rbase = te.y, rmask = p.R - 1, mbase = 128 * (u & 1) + 64 * w;
-            // ---------------- phase 1: P^T
+            // ---------------- phase 1: P^T, in two halves of 32 query columns: the dV MMAs of
+            // the first half run while the second is exponentiated
             float pf[64];
             {
                 uint32_t sv[2][32];
                 tmem_ld32(tmem + lane_off + cS + 64 * w, sv[0]);
+                tmem_wait_ld_regs(sv[0]);
                 tmem_ld32(tmem + lane_off + cS + 64 * w + 32, sv[1]);
-                tmem_wait_ld();
-                // all 64 columns branch-free, two at a time; masks (rows outside the entry, the
-                // causal triangle) in a separate pass only where some lane needs them
                 const uint64_t sc2 = f2_pack(sl2, sl2);
+                const bool need_mask = causal || __any_sync(0xffffffffu, !row_in);
 #pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 l4 = ls4[i4];       // -lse * log2(e) of four query columns
-                    float x0, x1, x2, x3;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i4 >> 3][4 * (i4 & 7)]), __uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + 1])),
-                                     sc2, f2_pack(l4.x, l4.y)), x0, x1);
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + 2]), __uint_as_float(sv[i4 >> 3][4 * (i4 & 7) + 3])),
-                                     sc2, f2_pack(l4.z, l4.w)), x2, x3);
-                    pf[4 * i4] = ex2(x0);
-                    pf[4 * i4 + 1] = ex2(x1);
-                    pf[4 * i4 + 2] = ex2(x2);
-                    pf[4 * i4 + 3] = ex2(x3);
-                }
-                if (causal || __any_sync(0xffffffffu, !row_in)) {
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1) tmem_wait_ld_regs(sv[1]);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int r = rbase + ((mbase + c) & rmask);
-                        pf[c] = (row_in && !(causal && jj > r)) ? pf[c] : 0.f;
+                    for (int i4 = 8 * h; i4 < 8 * h + 8; ++i4) {
+                        const float4 l4 = ls4[i4];       // -lse * log2(e) of four query columns
+                        float x0, x1, x2, x3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[h][4 * (i4 & 7)]), __uint_as_float(sv[h][4 * (i4 & 7) + 1])),
+                                         sc2, f2_pack(l4.x, l4.y)), x0, x1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[h][4 * (i4 & 7) + 2]), __uint_as_float(sv[h][4 * (i4 & 7) + 3])),
+                                         sc2, f2_pack(l4.z, l4.w)), x2, x3);
+                        pf[4 * i4] = ex2(x0);
+                        pf[4 * i4 + 1] = ex2(x1);
+                        pf[4 * i4 + 2] = ex2(x2);
+                        pf[4 * i4 + 3] = ex2(x3);
                     }
-                }
-                uint32_t pk[2][16];
+                    if (need_mask) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i >> 4][i & 15] = pack_bf16(pf[2 * i], pf[2 * i + 1]);
-                tmem_st16(tmem + lane_off + cS + 64 * w, pk[0]);
-                tmem_st16(tmem + lane_off + cS + 64 * w + 16, pk[1]);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
+                        for (int c = 32 * h; c < 32 * h + 32; ++c) {
+                            const int r = rbase + ((mbase + c) & rmask);
+                            pf[c] = (row_in && !(causal && jj > r)) ? pf[c] : 0.f;
+                        }
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pf[32 * h + 2 * i], pf[32 * h + 2 * i + 1]);
+                    tmem_st16(tmem + lane_off + cS + 64 * w + 16 * h, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(h == 0 ? p_full : p_half1);
+                }
             }
             // ---------------- phase 2: dS^T
             ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1, abort, p.status) &&

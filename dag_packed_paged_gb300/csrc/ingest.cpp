@@ -28,6 +28,7 @@ extern "C" int tree_attn_ingest(const int32_t *tokens, const int64_t *offsets, i
                                 ta_branch *branches, int32_t max_branches, int32_t *n_branches,
                                 int32_t *row_tokens, int64_t max_rows, int64_t *n_rows, int64_t *row_of,
                                 int32_t *row_owner) {
+    treeattn::NvtxRange nvtx_range("tree_attn_ingest");
     if (n_traj < 0 || !offsets || !n_branches || !n_rows || (n_traj > 0 && !row_of)) {
         set_error("tree_attn_ingest: bad arguments");
         return TA_ERR_INVALID;

@@ -63,6 +63,7 @@ int scratch_address(const ta_plan *plan, void **out) {
 extern "C" int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
                                      const void *o, const float *lse, const void *d_o, float *dq, float *dk_pool,
                                      float *dv_pool, void *stream) {
+    treeattn::NvtxRange nvtx_range("tree_attn_bwd_noalloc");
     using namespace treeattn;
     if (!plan) {
         set_error("tree_attn_bwd_noalloc: plan is NULL");

@@ -322,6 +322,7 @@ using namespace treeattn;
 extern "C" int tree_attn_place(const int32_t *tokens, const int64_t *offsets, int32_t n_traj, const ta_place_config *cfg,
                                int32_t *microbatch_of, int32_t *replica_of, int32_t *slot_of, int64_t *mb_work,
                                ta_place_stats *stats) {
+    treeattn::NvtxRange nvtx_range("tree_attn_place");
     if (!cfg || !offsets || n_traj <= 0 || !microbatch_of || !replica_of || !slot_of || !stats) {
         set_error("tree_attn_place: NULL argument or no trajectories");
         return TA_ERR_INVALID;

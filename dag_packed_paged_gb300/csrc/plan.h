@@ -5,9 +5,20 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/treeattn.h"
 
 namespace treeattn {
+
+// Names one call of the library on a profiler's timeline (Nsight Systems, ncu's NVTX filter).
+// NVTX v3 is header-only: with no tool attached a push/pop costs a few nanoseconds.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 constexpr int kTileRows = 128;       // key rows per tile (the N of S = Q K^T, the K of O = P V)
 constexpr int kBlockMRows = 256;     // query (row, head) pairs per query block: two 128-lane tiles
