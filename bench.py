@@ -46,7 +46,7 @@ DESCRIPTION = {
 }
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 NOMINAL_BF16_TFLOPS = 2250.0   # GB300 dense bf16 tensor-core peak, nominal (the measured peaks are the denominators)
-KERNEL_SOURCES = {"dkdv": "bwd.cu", "dq": "bwd.cu", "fwd": "fwd.cu"}
+KERNEL_SOURCES = {"dkdv": "bwd.cu", "dq": "bwd.cu", "fwd": "fwd_pair.cu"}
 
 
 def log(*a):

@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtreeattn.so")
-SOURCES = ["plan.cpp", "ingest.cpp", "place.cpp", "api.cu", "fwd.cu", "bwd.cu", "rope.cu", "logprob.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["plan.cpp", "ingest.cpp", "place.cpp", "api.cu", "fwd.cu", "fwd_pair.cu", "bwd.cu", "rope.cu", "logprob.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -360,7 +360,7 @@ cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const KvMaps &kv, const FwdPar
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
                        cudaStream_t stream, void *const *trace) {
     if (D == 64) return launch_fwd_d<64>(tm_q, kv, p, n_blocks, stream, trace);
-    return launch_fwd_d<128>(tm_q, kv, p, n_blocks, stream, trace);
+    return launch_fwd_pair(tm_q, kv, p, n_blocks, stream, trace);
 }
 
 }  // namespace treeattn

@@ -90,6 +90,10 @@ struct KvMaps {
 cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
                        cudaStream_t stream, void *const *trace);
 
+// The forward on CTA pairs (head dim 128; see fwd_pair.cu); launch_fwd dispatches to it.
+cudaError_t launch_fwd_pair(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
+                            cudaStream_t stream, void *const *trace);
+
 cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const CUtensorMap &tm_do,
                        const BwdParams &p, int n_blocks, int n_chunks, int n_reduce, cudaStream_t stream,
                        void *const *trace);
