@@ -5,7 +5,7 @@ in include/treeattn.h); this package is its Python binding.  Importing the packa
 load the library; the first call does, and raises if it has not been built.
 """
 from ._native import (  # noqa: F401
-    TA_CLAMP_MOUNTS, TA_ERR_CUDA, TA_ERR_DEVICE_TIMEOUT, TA_ERR_INVALID, TA_ERR_NOMEM,
+    TA_CLAMP_MOUNTS, TA_ERR_CUDA, TA_ERR_DEVICE_BOUNDS, TA_ERR_DEVICE_TIMEOUT, TA_ERR_INVALID, TA_ERR_NOMEM,
     TA_ERR_UNSUPPORTED, TA_NO_MOUNTS, TA_OK, TA_PLAN_HOST_ONLY, TA_PLAN_STREAM_ORDERED, TA_TRANSITIVE_MOUNTS, Plan,
     TreeAttnError, tree_attn_bwd,
     tree_attn_bwd_noalloc,

@@ -11,7 +11,11 @@ import re
 
 import numpy as np
 
-from .build import LIB, INCLUDE
+from .build import LIB as _LIB_RELEASE, LIB_DEBUG, INCLUDE
+
+# TREEATTN_DEBUG=1 selects the TA_DEBUG build (device-side bounds checks; build it with
+# dag_packed_paged_gb300.build.build(debug=True)).
+LIB = LIB_DEBUG if os.environ.get("TREEATTN_DEBUG") == "1" else _LIB_RELEASE
 
 # numpy view of ta_branch (int32 parent, fork_offset, length; int64 row_start; C alignment)
 BRANCH_DTYPE = np.dtype(
@@ -23,6 +27,7 @@ TA_ERR_UNSUPPORTED = -2
 TA_ERR_NOMEM = -3
 TA_ERR_CUDA = -4
 TA_ERR_DEVICE_TIMEOUT = -5
+TA_ERR_DEVICE_BOUNDS = -6
 TA_CLAMP_MOUNTS = 0x1
 TA_NO_MOUNTS = 0x2
 TA_TRANSITIVE_MOUNTS = 0x4

@@ -11,6 +11,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtreeattn.so")
+# The same library compiled with -DTA_DEBUG: every kernel checks its page-table lookups, TMA
+# pool rows and output rows on the device and reports a failed check through the plan's status
+# word (tree_attn_check: TA_ERR_DEVICE_BOUNDS) instead of touching memory out of range.  Loaded
+# instead of LIB when TREEATTN_DEBUG=1.
+LIB_DEBUG = os.path.join(BUILD, "libtreeattn_debug.so")
 SOURCES = ["plan.cpp", "ingest.cpp", "place.cpp", "api.cu", "fwd.cu", "fwd_pair.cu", "bwd.cu", "rope.cu", "logprob.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -28,14 +33,15 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
-        return LIB
+    out = LIB_DEBUG if debug else LIB
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= _deps():
+        return out
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                     "--expt-relaxed-constexpr"]
-    tag = f"{os.getpid()}"
+                     "--expt-relaxed-constexpr"] + (["-DTA_DEBUG"] if debug else [])
+    tag = f"{os.getpid()}{'d' if debug else ''}"
 
     def compile_one(src):
         obj = os.path.join(BUILD, src + f".{tag}.o")
@@ -51,16 +57,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".{tag}.tmp"
+    tmp = out + f".{tag}.tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
         "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     for o in objs:
         os.remove(o)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":

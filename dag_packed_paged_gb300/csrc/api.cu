@@ -437,6 +437,11 @@ int tree_attn_check(const ta_plan *plan, void *stream) {
             set_error("a bounded device-side wait expired; outputs of the affected launches are invalid");
             return TA_ERR_DEVICE_TIMEOUT;
         }
+        if (any & kStatusBounds) {
+            set_error("a device-side bounds check (TA_DEBUG build) found a page index, pool row or output row "
+                      "out of range; the access was skipped and the outputs are invalid");
+            return TA_ERR_DEVICE_BOUNDS;
+        }
         set_error("a kernel found its dynamic shared memory misaligned and did nothing; outputs are invalid");
         return TA_ERR_CUDA;
     }
@@ -514,6 +519,9 @@ int tree_attn_rope(const ta_plan *plan, void *q, void *k_pool, double theta_base
     p.Hq = h.cfg.num_q_heads;
     p.Hkv = h.cfg.num_kv_heads;
     p.page_size = h.cfg.page_size;
+    p.n_logical_pages = h.n_logical_pages;
+    p.num_pages = h.cfg.num_pages;
+    p.status = plan->d_status + 2;
     for (int i = 0; i < D / 2; ++i) p.inv_freq[i] = std::pow(theta_base, -2.0 * i / D);
     cudaError_t e = launch_rope(D, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TA_OK : cuda_fail(e, "rope launch");

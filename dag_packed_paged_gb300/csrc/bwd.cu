@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(128) delta_kernel(const BwdParams p) {
     const int m = threadIdx.x, m_flat = 128 * t + m;
     const int hl = m_flat / p.R, rl = m_flat % p.R, h = g * p.G + hl;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
-    const bool valid = rl < n_rows;
+    const bool valid = rl < n_rows && debug_in_range(q_row0 + rl, 0, p.N, p.status);
     float nlse2 = -INFINITY, acc = 0.f;
     if (valid) {
         const int r = q_row0 + rl;
@@ -270,7 +270,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         int k_issued = 0, v_issued = 0;
         for (int j = 0; j < E; ++j) {
             if ((j & 31) == 0)
-                pack_feed_fill(f, j, E, tiles, p.page_table, p.n_logical_pages, p.page_size, oob, lane);
+                pack_feed_fill(f, j, E, tiles, p.page_table, p.n_logical_pages, p.page_size, oob, lane, p.status);
             int y[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, f.y[i], j & 31);
@@ -362,7 +362,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const int m_flat = 128 * t + 32 * q4 + lane;
         const int hl = m_flat / p.R, rl = m_flat % p.R;
         const int r_abs = q_row0 + rl, h = g * p.G + hl;
-        const bool valid = rl < n_rows;
+        const bool valid = rl < n_rows && debug_in_range(r_abs, 0, p.N, p.status);
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         // the two groups put this lane's Q row into TMEM, half each
         row_to_tmem<D>(tmem + lane_off + cQ, p.q + (static_cast<size_t>(r_abs) * p.Hq + h) * D, valid, w);
@@ -597,7 +597,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int ppt = kTileRows / p.page_size;
         int ky[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ky[i] = i < ppt ? __ldg(p.tile_rows + tile * ppt + i) : 0;
+        for (int i = 0; i < 8; ++i) {
+            ky[i] = i < ppt ? __ldg(p.tile_rows + tile * ppt + i) : 0;
+            // (TA_DEBUG) a pool row outside the pool reads the zero-filled row past it instead
+            if (!debug_in_range(ky[i], 0, static_cast<long long>(p.num_pages) * p.page_size, p.status))
+                ky[i] = p.num_pages * p.page_size;
+        }
         if (lane == 0) {
             tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
             tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
@@ -815,7 +820,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             } else {
                 write = jj < p.N;
                 const int l = jj / p.page_size;
-                const size_t prow = write ? static_cast<size_t>(__ldg(p.page_table + l)) * p.page_size + jj % p.page_size : 0;
+                write = write && debug_in_range(l, 0, p.n_logical_pages, p.status);
+                const int pg = write ? __ldg(p.page_table + l) : 0;
+                write = write && debug_in_range(pg, 0, p.num_pages, p.status);
+                const size_t prow = write ? static_cast<size_t>(pg) * p.page_size + jj % p.page_size : 0;
                 dst = (w == 0 ? p.dk_pool : p.dv_pool) + (prow * p.Hkv + g) * D;
             }
             const float mul = w == 0 ? p.scale : 1.f;
@@ -862,7 +870,10 @@ __global__ void __launch_bounds__(256) reduce_kernel(const BwdParams p) {
                 p.partials + ((static_cast<size_t>(s0 + s) * p.Hkv + g) * 2 + which) * kTileRows * D)[row * V4 + c4];
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
-        const size_t prow = static_cast<size_t>(__ldg(p.page_table + jj / p.page_size)) * p.page_size + jj % p.page_size;
+        if (!debug_in_range(jj / p.page_size, 0, p.n_logical_pages, p.status)) continue;
+        const int pg = __ldg(p.page_table + jj / p.page_size);
+        if (!debug_in_range(pg, 0, p.num_pages, p.status)) continue;
+        const size_t prow = static_cast<size_t>(pg) * p.page_size + jj % p.page_size;
         float *dst = (which == 0 ? p.dk_pool : p.dv_pool) + (prow * p.Hkv + g) * D;
         reinterpret_cast<float4 *>(dst)[c4] = acc;
     }

@@ -151,7 +151,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int issued = 0;
         for (int j = 0; j < E; ++j) {
             if ((j & 31) == 0)
-                pack_feed_fill(f, j, E, tiles, p.page_table, p.n_logical_pages, p.page_size, oob, lane);
+                pack_feed_fill(f, j, E, tiles, p.page_table, p.n_logical_pages, p.page_size, oob, lane, p.status);
             int y[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, f.y[i], j & 31);
@@ -379,7 +379,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
             tc_fence_after();
-            const bool valid = rl < n_rows;
+            const bool valid = rl < n_rows && debug_in_range(r_abs, 0, p.N, p.status);
             const int hh = g * p.G + hl;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = p.o + (static_cast<size_t>(r_abs) * p.Hq + hh) * D;

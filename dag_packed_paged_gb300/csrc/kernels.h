@@ -68,6 +68,8 @@ struct RopeParams {
     const int32_t *page_table;  // logical page -> pool page
     int64_t N;
     int32_t Hq, Hkv, page_size;
+    int64_t n_logical_pages, num_pages;   // bounds of the page table and the pool (TA_DEBUG checks)
+    int *status;                // status word of the plan (TA_DEBUG checks)
     double inv_freq[64];        // theta_base^(-2i/D), i < D/2
 };
 

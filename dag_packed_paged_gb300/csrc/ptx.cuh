@@ -16,6 +16,26 @@ constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s per wait, then gi
 // status bits (device word, read by tree_attn_check)
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusMisaligned = 2;   // dynamic shared memory not 1024-byte aligned: kernel did nothing
+constexpr int kStatusBounds = 4;       // TA_DEBUG builds: a plan index or TMA row was out of range (access skipped)
+
+// TA_DEBUG builds check every plan-derived page index, pool row and output row on the device
+// before using it: an index out of [lo, hi) raises kStatusBounds and the caller skips the access
+// (a load reads the zero-filled row past the pool instead).  Release builds compile the checks
+// away and always return true.
+__device__ __forceinline__ bool debug_in_range(long long v, long long lo, long long hi, int *status) {
+#ifdef TA_DEBUG
+    if (v < lo || v >= hi) {
+        atomicOr(status, kStatusBounds);
+        return false;
+    }
+#else
+    (void)v;
+    (void)lo;
+    (void)hi;
+    (void)status;
+#endif
+    return true;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -405,12 +425,33 @@ struct PackFeed {
 
 __device__ __forceinline__ void pack_feed_fill(PackFeed &f, int base, int n, const int4 *tiles,
                                                const int32_t *page_table, int n_logical, int P, int oob_row,
-                                               int lane) {
+                                               int lane, int *status) {
     const int j = base + lane;
     if (j < n) {
         f.a = __ldg(tiles + 2 * j);
         f.b = __ldg(tiles + 2 * j + 1);
         const int pc[4] = {f.a.x, f.a.y, f.a.z, f.a.w};
+#ifdef TA_DEBUG
+        // a piece's logical page must exist and map into the pool; otherwise its rows read zeros
+        const int num_pages = oob_row / P;
+        auto row_of = [&](int li, int off) {
+            if (!debug_in_range(li, 0, n_logical, status)) return oob_row;
+            const int pg = __ldg(page_table + li);
+            return debug_in_range(pg, 0, num_pages, status) ? pg * P + off : oob_row;
+        };
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int p = pc[k];
+            if (P >= 32) {
+                f.y[2 * k] = p >= 0 ? row_of((32 * p) / P, (32 * p) % P) : oob_row;
+                f.y[2 * k + 1] = oob_row;
+            } else {
+                f.y[2 * k] = p >= 0 ? row_of(2 * p, 0) : oob_row;
+                f.y[2 * k + 1] = (p >= 0 && 2 * p + 1 < n_logical) ? row_of(2 * p + 1, 0) : oob_row;
+            }
+        }
+#else
+        (void)status;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int p = pc[k];
@@ -422,6 +463,7 @@ __device__ __forceinline__ void pack_feed_fill(PackFeed &f, int base, int n, con
                 f.y[2 * k + 1] = (p >= 0 && 2 * p + 1 < n_logical) ? __ldg(page_table + 2 * p + 1) * P : oob_row;
             }
         }
+#endif
     }
 }
 

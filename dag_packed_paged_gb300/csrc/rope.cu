@@ -12,6 +12,7 @@
 // all Hq + Hkv heads.  The angle is formed and reduced mod 2 pi in fp64 (positions reach 2^18
 // and beyond, where an fp32 product would be off by ~1e-2 rad), the sine and cosine in fp32.
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace treeattn {
 
@@ -43,7 +44,10 @@ __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p) {
     };
     __nv_bfloat16 *qrow = p.q + r * p.Hq * D;
     for (int h = hsub; h < p.Hq; h += kHpw) rotate(qrow + h * D);
-    const int64_t prow = static_cast<int64_t>(__ldg(p.page_table + r / p.page_size)) * p.page_size + r % p.page_size;
+    if (!debug_in_range(r / p.page_size, 0, p.n_logical_pages, p.status)) return;
+    const int pg = __ldg(p.page_table + r / p.page_size);
+    if (!debug_in_range(pg, 0, p.num_pages, p.status)) return;
+    const int64_t prow = static_cast<int64_t>(pg) * p.page_size + r % p.page_size;
     __nv_bfloat16 *krow = p.k_pool + prow * p.Hkv * D;
     for (int h = hsub; h < p.Hkv; h += kHpw) rotate(krow + h * D);
 }

@@ -39,6 +39,9 @@ extern "C" {
 #define TA_ERR_NOMEM (-3)           /* host or device allocation failed (planner only) */
 #define TA_ERR_CUDA (-4)            /* a CUDA runtime/driver call failed */
 #define TA_ERR_DEVICE_TIMEOUT (-5)  /* a bounded device-side wait expired; outputs are invalid */
+#define TA_ERR_DEVICE_BOUNDS (-6)   /* a device-side bounds check of the TA_DEBUG build failed (a
+                                       page index, pool row or output row out of range; the
+                                       access was skipped); outputs are invalid */
 
 /* Flags (ta_config.flags). */
 #define TA_CLAMP_MOUNTS 0x1u  /* clamp a mount span to the source's rows instead of rejecting it
@@ -450,8 +453,11 @@ int tree_attn_bwd_noalloc(const ta_plan *plan, const void *q, const void *k_pool
 size_t tree_attn_bwd_workspace_size(const ta_plan *plan);
 
 /* Synchronises `stream` and reports whether any bounded device wait of this plan's kernels
- * expired since the last check (TA_ERR_DEVICE_TIMEOUT) or a CUDA error is pending
- * (TA_ERR_CUDA); clears the status with a copy on `stream` (other streams are not waited for). */
+ * expired since the last check (TA_ERR_DEVICE_TIMEOUT), a device-side bounds check failed
+ * (TA_ERR_DEVICE_BOUNDS; only the library built with TA_DEBUG, libtreeattn_debug.so, checks:
+ * every page-table lookup, TMA pool row and output row of its kernels, skipping the access and
+ * setting a status bit instead of faulting) or a CUDA error is pending (TA_ERR_CUDA); clears
+ * the status with a copy on `stream` (other streams are not waited for). */
 int tree_attn_check(const ta_plan *plan, void *stream);
 
 /* Diagnostic: runs the bounded-wait error path on purpose.  Launches one kernel on `stream`

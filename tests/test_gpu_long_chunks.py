@@ -5,8 +5,9 @@ refill their copies of the reader list every 32 entries, and the Q/dO rings wrap
 times on a long chunk.  These tests compare every element of dQ, dK and dV with the fp64 oracle on
 episodes whose chunks are long -- by shape (the mount-heavy workload at 1/8 size, a wide fan),
 by forcing unsplit chunks through ta_config.dkdv_chunk_entries, and at full size on the rows of
-one mount-heavy DAG that gather from the most readers (stored oracle values, written by
-tests/golden/make_mount_heavy_dkdv.py).  References: Octopus Section 3.4 (differentiable mount
+one mount-heavy DAG that gather from the most readers and of the balanced tree's root and first
+depth-1 edge (stored oracle values, written by tests/golden/make_mount_heavy_dkdv.py and
+make_balanced_tree_dkdv.py).  References: Octopus Section 3.4 (differentiable mount
 edges) and HARTS Section 3.4 (the gather backward accumulates every consumer into the unique
 compact row)."""
 import hashlib
@@ -23,6 +24,7 @@ from gpu_helpers import Run, assert_close
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "mount_heavy_dag0_dkdv.npz")
+GOLDEN_BT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "balanced_tree_dkdv.npz")
 
 
 def _longest_chunk(plan):
@@ -107,3 +109,27 @@ def test_mount_heavy_full_size_shared_rows():
     for name, got, want in (("dK", dk, g["dk"]), ("dV", dv, g["dv"])):
         assert_close(name + " span", got[rows[span]], want[span].astype(np.float64))
         assert_close(name + " root", got[rows[~span]], want[~span].astype(np.float64))
+
+
+def test_balanced_tree_full_size_shared_rows():
+    """Full-size balanced tree in the benchmark's launch configuration: dK and dV of 32 rows of
+    the 4,096-row root (read by all 45,056 rows) and 32 rows of the first depth-1 edge (read by
+    its 10,240-row subtree), against the oracle over the whole tree."""
+    if not os.path.exists(GOLDEN_BT):
+        pytest.fail(f"{GOLDEN_BT} is missing; run tests/golden/make_balanced_tree_dkdv.py")
+    g = np.load(GOLDEN_BT)
+    ep = W.config(1)
+    run = Run(ep)
+    h = hashlib.sha256()
+    for a in (ep.branches, ep.mounts, run.t.q, run.t.k, run.t.v, run.t.do):
+        h.update(np.ascontiguousarray(a).tobytes())
+    assert h.hexdigest() == str(g["input_sha256"]), "the stored oracle values are for other inputs"
+    run.fwd()
+    dq, dk, dv = run.bwd()
+    rows = g["rows"]
+    lo, hi = (int(x) for x in g["edge"])
+    edge = (rows >= lo) & (rows < hi)
+    assert edge.sum() == 32 and (rows < int(ep.branches["length"][0])).sum() == 32
+    for name, got, want in (("dK", dk, g["dk"]), ("dV", dv, g["dv"])):
+        assert_close(name + " root", got[rows[~edge]], want[~edge].astype(np.float64))
+        assert_close(name + " edge", got[rows[edge]], want[edge].astype(np.float64))
