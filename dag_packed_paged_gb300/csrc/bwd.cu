@@ -89,7 +89,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sA, uint32_t 
     }
 }
 
-constexpr int kDqThreads = 352;    // dQ: warps 0-3 / 4-7 elementwise groups, 8 loads, 9 and 10 MMA
+constexpr int kDqThreads = 384;    // dQ: warps 0-3 / 4-7 elementwise groups, 8 loads, 9 / 10 / 11 MMA (S, dP, dQ)
 constexpr int kDkvThreads = 352;   // dK/dV: warps 9 and 10 each issue one of the two MMA chains
 constexpr int kQStages = 3;        // dK/dV: Q stages (a Q tile is last read by dK)
 constexpr int kDoStages = 2;       // dK/dV: dO stages (a dO tile is last read by dV)
@@ -190,10 +190,12 @@ struct DqLayout {
 //   MMA:  dQ += dS_j K_j
 // dS has TMEM columns of its own, so no MMA of entry j + 1 waits for dQ_j: while the
 // elementwise groups work on entry j the tensor core runs S_{j+1}, dP_{j+1} and dQ_{j-1}.
-// Two threads issue the MMAs -- warp 9: S and dQ, warp 10: dP -- because issuing a batch
-// blocks the thread while the tensor core's queue is full, and a single issuer then reacts
-// to the elementwise groups' signals late (one issuer: 27.3 ms on the mount-heavy workload,
-// two: 21.6 ms; three, or S+dP / dQ, or S / dP+dQ: 22.7 to 23.5 ms).
+// Three threads issue the MMAs -- warp 9: S, warp 10: dP, warp 11: dQ -- because issuing a
+// batch blocks the thread while the tensor core's queue is full, and an issuer that also
+// waits for dS_j would start S_{j+2} only after dQ_j (on the mount-heavy workload: one issuer
+// 27.3 ms; S and dQ on one thread, dP on another, 23.0 ms; three issuers 21.65 ms, dQ
+// bit-identical).  K_j is freed by the dQ issuer's commit: S_j, its other reader, finished
+// before the groups could form dS_j.
 // The two groups split each entry's 128 key columns (64 each); P stays in their registers
 // between the phases.
 template <int D>
@@ -237,7 +239,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         mbar_init(dp_free, 8);
         mbar_init(ds_full, 8);
         mbar_init(ds_free, 1);
-        mbar_init(o_full, 2);                 // one commit from each MMA issuer
+        mbar_init(o_full, 3);                 // one commit from each MMA issuer
         *abort = 0;
         fence_barrier_init();
     }
@@ -301,29 +303,38 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 mbar_wait(v_full(d % kVStages), (d / kVStages) & 1, nullptr, p.status);
         }
     } else if (warp == 9) {
-        // ---------------------------------------------------------------- MMA: S and dQ
+        // ---------------------------------------------------------------- MMA: S
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
             bool ok = E > 0 && mbar_wait(q_ready, 0, abort, p.status) && mbar_wait(k_full(0), 0, abort, p.status);
             if (ok) {
                 tc_fence_after();
                 issue_tk<D>(tmem + cS, tmem + cQ, sK, idesc_s);        // S_0 = Q K_0^T
                 mma_commit(s_full);
             }
+            for (int j = 0; ok && j + 1 < E; ++j) {
+                const int ks1 = (j + 1) % kKStages;
+                // S_{j+1} as soon as both groups have read S_j
+                if (!(ok = mbar_wait(s_free, j & 1, abort, p.status) &&
+                           mbar_wait(k_full(ks1), ((j + 1) / kKStages) & 1, abort, p.status)))
+                    break;
+                tc_fence_after();
+                issue_tk<D>(tmem + cS, tmem + cQ, sK + ks1 * L::kTile, idesc_s);
+                mma_commit(s_full);
+            }
+            mma_commit(o_full);
+            mbar_wait(o_full, 0, nullptr, p.status);
+        }
+    } else if (warp == 11) {
+        // ---------------------------------------------------------------- MMA: dQ
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
+            bool ok = true;
             for (int j = 0; ok && j < E; ++j) {
-                const int ks = j % kKStages, ks1 = (j + 1) % kKStages;
-                if (j + 1 < E) {
-                    // S_{j+1} as soon as both groups have read S_j
-                    if (!(ok = mbar_wait(s_free, j & 1, abort, p.status) &&
-                               mbar_wait(k_full(ks1), ((j + 1) / kKStages) & 1, abort, p.status)))
-                        break;
-                    tc_fence_after();
-                    issue_tk<D>(tmem + cS, tmem + cQ, sK + ks1 * L::kTile, idesc_s);
-                    mma_commit(s_full);
-                }
+                const int ks = j % kKStages;
                 if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status))) break;
                 tc_fence_after();
+                // S_j, the other reader of K_j, finished before the groups could form dS_j
                 issue_acc(tmem + cDQ, tmem + cDS, sK + ks * L::kTile, idesc_o, j > 0);   // dQ += dS_j K_j
                 mma_commit(k_empty(ks));
                 mma_commit(ds_free);
