@@ -96,3 +96,21 @@ def test_fwd_full_size_sampled_rows(cfg):
     assert_close("O", o[rows], ref.o)
     assert metrics(lse[rows], ref.lse)[0] <= 2e-3
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("heads,page", [((4, 1), 16), ((16, 4), 16), ((8, 1), 32)], ids=["G4-P16", "G4x4-P16", "G8-P32"])
+def test_fwd_bwd_head_dim_128_small_pages(heads, page):
+    """Head dim 128 (the CTA-pair forward) on 16- and 32-row pages: a 32-row slot of a packed key
+    tile is then two pages (two TMA boxes per CTA half), or one box per slot with no 64-row
+    halves -- the load paths the page-64 workloads do not take."""
+    ep = W.random_small(3000 + page + heads[0], max_branches=8, max_len=700, heads=heads, head_dim=128,
+                        page_size=page, n_mounts=3)
+    run = Run(ep, dist="realistic")
+    o, lse = run.fwd()
+    dq, dk, dv = run.bwd()
+    ref = oracle.run(ep.branches, ep.mounts, run.t.q, run.t.k, run.t.v, run.t.do, ep.softmax_scale)
+    assert_close("O", o, ref.o)
+    assert metrics(lse, ref.lse)[0] <= 2e-3
+    assert_close("dQ", dq, ref.dq)
+    assert_close("dK", dk, ref.dk)
+    assert_close("dV", dv, ref.dv)
