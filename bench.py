@@ -667,6 +667,17 @@ def main():
         "gpu_launches": K * (1 + 3 + (1 if n_reduce else 0)),
         "e2e": e2e,
     }
+    # achieved DRAM rate of each attention kernel (the forward's is the paged K/V gather): the
+    # bytes per launch of the committed ncu capture, when it matches the current source, over the
+    # kernel's time measured above
+    dram = {}
+    for k in ("fwd", "dq", "dkdv"):
+        b = recorded_traffic(k, args.workload)
+        if b is not None:
+            gbs = b / kern_ms[k] / 1e6
+            dram[k] = {"bytes_per_launch": b, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+    if dram:
+        line["dram"] = dict(dram, peak_gbs=peaks["hbm_gbs"], peak_kind=f"HBM copy ({peak_kind})")
     if rank == 0:
         line["clocks"] = clocks.summary()
         others = [w for w in args.also.split(",") if w and w != args.workload] if world == 1 else []
