@@ -565,7 +565,8 @@ def main():
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     achieved = algo[dominant] / kern_ms[dominant] / 1e9
-    traffic = recorded_traffic(dominant, args.workload)
+    # the committed DRAM bytes are for the full-size workload: a --scale run reports none
+    traffic = recorded_traffic(dominant, args.workload) if args.scale == 1 else None
     value = (flops_fwd + flops_bwd) * world / ms / 1e9
     fwd_tflops = flops_fwd / kern_ms["fwd"] / 1e9
 
@@ -672,7 +673,7 @@ def main():
     # kernel's time measured above
     dram = {}
     for k in ("fwd", "dq", "dkdv"):
-        b = recorded_traffic(k, args.workload)
+        b = recorded_traffic(k, args.workload) if args.scale == 1 else None
         if b is not None:
             gbs = b / kern_ms[k] / 1e6
             dram[k] = {"bytes_per_launch": b, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
