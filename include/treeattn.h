@@ -396,6 +396,10 @@ int tree_attn_logprob_index(const int64_t *pos_row, const int32_t *pos_target, i
  * launch failure.  A bounded device-side wait that expires inside the
  * launched kernels is not seen by this call: it is recorded in the plan's status words and
  * reported by the next tree_attn_check on the plan (TA_ERR_DEVICE_TIMEOUT).
+ * Because the call only enqueues kernels, it can be recorded by CUDA stream capture: a graph
+ * holding several layers' tree_attn_fwd and tree_attn_bwd calls on one plan replays them with
+ * one launch, as long as the plan, the tensors and the workspace stay alive (tree_attn_check
+ * synchronises and belongs outside the capture).
  */
 int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const void *v_pool,
                   void *o, float *lse, void *stream);
