@@ -46,7 +46,7 @@ DESCRIPTION = {
 }
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 NOMINAL_BF16_TFLOPS = 2250.0   # GB300 dense bf16 tensor-core peak, nominal (the measured peaks are the denominators)
-KERNEL_SOURCES = {"dkdv": "bwd.cu", "dq": "bwd.cu", "fwd": "fwd_pair.cu"}
+KERNEL_SOURCES = {"dkdv": ("bwd.cu",), "dq": ("bwd.cu",), "fwd": ("fwd_pair.cu", "fwd_store.cuh")}
 
 
 def log(*a):
@@ -62,10 +62,9 @@ def load_peaks():
 
 
 def kernel_hash(kernel):
-    src = os.path.join(ROOT, "dag_packed_paged_gb300", "csrc", KERNEL_SOURCES[kernel])
     h = hashlib.sha256()
-    for f in (src, os.path.join(ROOT, "dag_packed_paged_gb300", "csrc", "ptx.cuh")):
-        h.update(open(f, "rb").read())
+    for f in KERNEL_SOURCES[kernel] + ("ptx.cuh",):
+        h.update(open(os.path.join(ROOT, "dag_packed_paged_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -433,7 +432,7 @@ def time_workload(name, args, dev, peaks):
            "fwd_frac_of_nominal": fwd_tflops / NOMINAL_BF16_TFLOPS,
            "fwdbwd_frac_of_nominal": fb_tflops / NOMINAL_BF16_TFLOPS,
            "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()}, "clocks": clocks.summary(),
-           "gpu_launches": K * (1 + 3 + (1 if st["n_partial_slots"] > 0 else 0))}
+           "gpu_launches": K * (1 + (1 if st["n_fwd_split"] > 0 else 0) + 3 + (1 if st["n_partial_slots"] > 0 else 0))}
     del plan
     torch.cuda.empty_cache()
     return out
@@ -556,6 +555,7 @@ def main():
         return sum(trace[k][a].elapsed_time(trace[k][b]) for k in range(K)) / K
 
     n_reduce = st["n_partial_slots"] > 0
+    n_fwd_split = st["n_fwd_split"] > 0
     kern_ms = {"fwd": avg(0, 1), "delta": avg(2, 3), "dq": avg(3, 4), "dkdv": avg(4, 5), "reduce": avg(5, 6)}
     flops_fwd, flops_bwd = st["fwd_flops"], st["bwd_flops"]
     base = ep.head_dim * ep.num_q_heads * st["pairs"]
@@ -665,7 +665,7 @@ def main():
                      "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": traffic,
                      "peak_kind": f"bf16 dense, sustained ({peak_kind})",
                      "algorithmic": f"{algo[dominant] / 1e12:.3f} TFLOP per launch ({2 * {'fwd': 2, 'dq': 3, 'dkdv': 4}[dominant]}*D*Hq*pairs)"},
-        "gpu_launches": K * (1 + 3 + (1 if n_reduce else 0)),
+        "gpu_launches": K * (1 + (1 if n_fwd_split else 0) + 3 + (1 if n_reduce else 0)),
         "e2e": e2e,
     }
     # achieved DRAM rate of each attention kernel (the forward's is the paged K/V gather): the

@@ -59,7 +59,7 @@ class ta_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("flags", ctypes.c_uint32),
                 ("num_pages", ctypes.c_int64), ("num_sms", ctypes.c_int32),
-                ("dkdv_chunk_entries", ctypes.c_int32)]
+                ("dkdv_chunk_entries", ctypes.c_int32), ("fwd_split_tiles", ctypes.c_int32)]
 
 
 class ta_plan_stats(ctypes.Structure):
@@ -72,7 +72,8 @@ class ta_plan_stats(ctypes.Structure):
                 ("tile_rows", ctypes.c_int32), ("bwd_workspace_bytes", ctypes.c_size_t),
                 ("plan_ms", ctypes.c_double), ("n_ftiles", ctypes.c_int64), ("chunk_cap", ctypes.c_int64),
                 ("num_sms", ctypes.c_int32),
-                ("device", ctypes.c_int32)]
+                ("device", ctypes.c_int32), ("n_fwd_items", ctypes.c_int64), ("n_fwd_split", ctypes.c_int64),
+                ("fwd_split_cap", ctypes.c_int64)]
 
 
 class ta_place_config(ctypes.Structure):
@@ -98,7 +99,9 @@ class ta_plan_arrays(ctypes.Structure):
                 ("n_chunks", ctypes.c_int64), ("pos_ids", _P32), ("blocks", _P32),
                 ("blk_iv_ptr", _P64), ("iv_lo", _P32), ("iv_hi", _P32), ("diag", _P32),
                 ("entries", _P32), ("t_entries", _P32), ("chunks", _P32), ("fwd_order", _P32),
-                ("n_ftiles", ctypes.c_int64), ("fblk_ptr", _P64), ("ftiles", _P32)]
+                ("n_ftiles", ctypes.c_int64), ("fblk_ptr", _P64), ("ftiles", _P32),
+                ("n_fwd_items", ctypes.c_int64), ("n_fwd_split", ctypes.c_int64),
+                ("fwd_items", _P32), ("fwd_combine", _P32)]
 
 
 _lib = None
@@ -215,16 +218,18 @@ class Plan:
 def tree_attn_plan(branches: np.ndarray, mounts: np.ndarray, page_table: np.ndarray, *,
                    num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                    num_pages: int, softmax_scale: float = 0.0, flags: int = 0,
-                   stream=None, num_sms: int = 0, dkdv_chunk_entries: int = 0) -> Plan:
+                   stream=None, num_sms: int = 0, dkdv_chunk_entries: int = 0,
+                   fwd_split_tiles: int = 0) -> Plan:
     """branches: structured array with fields parent, fork_offset, length, row_start (the
     ta_branch layout); mounts: reader, reader_offset, source, src_begin, src_end.
-    num_sms / dkdv_chunk_entries: the dK/dV work-balance knobs of ta_config (0: defaults)."""
+    num_sms / dkdv_chunk_entries / fwd_split_tiles: the work-balance knobs of ta_config
+    (0: defaults; fwd_split_tiles < 0 never splits a forward block)."""
     br = np.ascontiguousarray(branches)
     mt = np.ascontiguousarray(mounts)
     assert br.dtype.itemsize == ctypes.sizeof(ta_branch) and mt.dtype.itemsize == ctypes.sizeof(ta_mount)
     pt = np.ascontiguousarray(page_table, dtype=np.int32)
     cfg = ta_config(num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale, flags, num_pages,
-                    num_sms, dkdv_chunk_entries)
+                    num_sms, dkdv_chunk_entries, fwd_split_tiles)
     n_rows = int((br["row_start"] + br["length"]).max()) if len(br) else 0
     pos = np.zeros(max(n_rows, 1), dtype=np.int32)
     h = ctypes.c_void_p()
@@ -314,6 +319,8 @@ def tree_attn_plan_export(plan: Plan) -> dict:
         "fwd_order": arr(a.fwd_order, nb),
         "fblk_ptr": arr(a.fblk_ptr, nb + 1, np.int64),
         "ftiles": arr(a.ftiles, 8 * a.n_ftiles).reshape(a.n_ftiles, 8),
+        "fwd_items": arr(a.fwd_items, 4 * a.n_fwd_items).reshape(a.n_fwd_items, 4),
+        "fwd_combine": arr(a.fwd_combine, 4 * a.n_fwd_split).reshape(a.n_fwd_split, 4),
     }
 
 

@@ -255,7 +255,7 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         fblk[2 * b] = int32_t(h.fblk_ptr[b]);
         fblk[2 * b + 1] = int32_t(h.fblk_ptr[b + 1]);
     }
-    Part parts[13] = {
+    Part parts[15] = {
         {h.blocks.data(), h.blocks.size() * 4, 0},   {h.entries.data(), h.entries.size() * 4, 0},
         {h.t_entries.data(), h.t_entries.size() * 4, 0}, {h.chunks.data(), h.chunks.size() * 4, 0},
         {h.fwd_order.data(), h.fwd_order.size() * 4, 0}, {h.reduce.data(), h.reduce.size() * 4, 0},
@@ -263,6 +263,7 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
         {h.tile_rows.data(), h.tile_rows.size() * 4, 0}, {h.t_info.data(), h.t_info.size() * 4, 0},
         {h.pos_ids.data(), h.pos_ids.size() * 4, 0},
         {h.ftiles.data(), h.ftiles.size() * 4, 0},     {fblk.data(), fblk.size() * 4, 0},
+        {h.fwd_items.data(), h.fwd_items.size() * 4, 0}, {h.fwd_combine.data(), h.fwd_combine.size() * 4, 0},
     };
     size_t total = 0;
     for (Part &p : parts) {
@@ -274,7 +275,7 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     plan->stream = stream;
     cudaError_t e = cudaSuccess;
     if (plan->stream_ordered) {
-        if ((rc = upload_stream_ordered(plan->device, &plan->d_buf, parts, 13, total, s))) {
+        if ((rc = upload_stream_ordered(plan->device, &plan->d_buf, parts, 15, total, s))) {
             delete plan;
             return rc;
         }
@@ -312,6 +313,23 @@ int tree_attn_plan(const ta_branch *branches, int32_t n_branches, const ta_mount
     plan->d_pos_ids = reinterpret_cast<const int32_t *>(d + parts[10].off);
     plan->d_ftiles = reinterpret_cast<const int32_t *>(d + parts[11].off);
     plan->d_fblk = reinterpret_cast<const int32_t *>(d + parts[12].off);
+    plan->d_fwd_items = reinterpret_cast<const int32_t *>(d + parts[13].off);
+    plan->d_fwd_combine = reinterpret_cast<const int32_t *>(d + parts[14].off);
+    // partial results of split forward blocks: written by the forward, read by the combine,
+    // never uploaded (an allocation of its own, in stream order like d_buf)
+    if (h.n_fwd_slots > 0) {
+        const size_t bytes = sizeof(float) * size_t(h.n_fwd_slots) * h.cfg.num_kv_heads * 256 * (h.cfg.head_dim + 1);
+        void *buf = nullptr;
+        e = plan->stream_ordered ? cudaMallocAsync(&buf, bytes, s) : cudaMalloc(&buf, bytes);
+        if (e != cudaSuccess) {
+            if (plan->stream_ordered) cudaFreeAsync(plan->d_buf, s);
+            else cudaFree(plan->d_buf);
+            delete plan;
+            return e == cudaErrorMemoryAllocation ? (set_error("device allocation failed"), TA_ERR_NOMEM)
+                                                  : cuda_fail(e, "plan allocation (split forward)");
+        }
+        plan->d_fwd_partial = static_cast<float *>(buf);
+    }
     *out = plan;
     return TA_OK;
 }
@@ -321,6 +339,10 @@ void tree_attn_plan_destroy(ta_plan *plan) {
     if (plan->d_buf) {
         if (plan->stream_ordered) cudaFreeAsync(plan->d_buf, static_cast<cudaStream_t>(plan->stream));
         else cudaFree(plan->d_buf);
+    }
+    if (plan->d_fwd_partial) {
+        if (plan->stream_ordered) cudaFreeAsync(plan->d_fwd_partial, static_cast<cudaStream_t>(plan->stream));
+        else cudaFree(plan->d_fwd_partial);
     }
     delete plan;
 }
@@ -362,6 +384,9 @@ int tree_attn_plan_stats(const ta_plan *plan, ta_plan_stats *out) {
     out->chunk_cap = h.chunk_cap;
     out->num_sms = h.num_sms;
     out->device = plan->device;
+    out->n_fwd_items = int64_t(h.fwd_items.size() / 4);
+    out->n_fwd_split = int64_t(h.fwd_combine.size() / 4);
+    out->fwd_split_cap = h.fwd_split_cap;
     return TA_OK;
 }
 
@@ -389,6 +414,10 @@ int tree_attn_plan_export(const ta_plan *plan, ta_plan_arrays *out) {
     out->n_ftiles = int64_t(h.ftiles.size() / kPackInts);
     out->fblk_ptr = h.fblk_ptr.data();
     out->ftiles = h.ftiles.data();
+    out->n_fwd_items = int64_t(h.fwd_items.size() / 4);
+    out->n_fwd_split = int64_t(h.fwd_combine.size() / 4);
+    out->fwd_items = h.fwd_items.data();
+    out->fwd_combine = h.fwd_combine.data();
     return TA_OK;
 }
 
@@ -549,8 +578,10 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     FwdParams p{};
     p.blocks = plan->d_blocks;
     p.ftiles = plan->d_ftiles;
-    p.fblk = plan->d_fblk;
-    p.order = plan->d_fwd_order;
+    p.items = plan->d_fwd_items;
+    p.combine = plan->d_fwd_combine;
+    p.partial = plan->d_fwd_partial;
+    p.n_slots = int32_t(h.n_fwd_slots);
     p.page_table = plan->d_page_table;
     p.tile_rows = plan->d_tile_rows;
     p.n_logical_pages = int32_t(h.n_logical_pages);
@@ -565,8 +596,8 @@ int tree_attn_fwd(const ta_plan *plan, const void *q, const void *k_pool, const 
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
     p.status = plan->d_status;
-    cudaError_t e = launch_fwd(h.cfg.head_dim, tm_q, kv, p, int(h.blocks.size() / 4),
-                               static_cast<cudaStream_t>(stream), plan->trace);
+    cudaError_t e = launch_fwd(h.cfg.head_dim, tm_q, kv, p, int(h.fwd_items.size() / 4),
+                               int(h.fwd_combine.size() / 4), static_cast<cudaStream_t>(stream), plan->trace);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attn_fwd launch");
     return TA_OK;
 }

@@ -8,8 +8,10 @@
 // and masking each slot's rows outside its [lo, hi) and, on slots of the block's own rows,
 // above the query row.
 //
-// One CTA = one query block (R rows x G heads = 256 query rows of the MMA, two 128-lane
-// tiles) x one KV head.  Warp roles:
+// One CTA = one work item (a query block, or a run of its packed tiles when the plan splits a
+// long block: split-KV) of R rows x G heads = 256 query rows of the MMA, two 128-lane tiles,
+// x one KV head.  A split item writes its normalised O and lse in fp32 to a partial slot, and
+// fwd_combine_kernel merges the parts.  Warp roles:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one (row, head) per thread)
 //   warps 4-7  softmax for query tile 1
 //   warp 8     TMA producer: Q once, then K and V tiles slot by slot (a box per 32-row slot,
@@ -20,6 +22,7 @@
 // The running max is rescaled lazily (only when it grows by more than 2^8).
 #include <cfloat>
 
+#include "fwd_store.cuh"
 #include "kernels.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -56,10 +59,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int qb = __ldg(p.order + blockIdx.x / p.Hkv);
+    const int4 item = __ldg(reinterpret_cast<const int4 *>(p.items) + blockIdx.x / p.Hkv);
+    const int qb = item.x, e0 = item.y, E = item.z - item.y, slot = item.w;
     const int g = blockIdx.x % p.Hkv;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
-    const int e0 = __ldg(p.fblk + 2 * qb), E = __ldg(p.fblk + 2 * qb + 1) - e0;
     const int4 *tiles = reinterpret_cast<const int4 *>(p.ftiles) + 2 * e0;   // two int4 per tile
 
     const uint32_t sQ = sbase + L::q_off, sK = sbase + L::k_off, sV = sbase + L::v_off;
@@ -309,27 +312,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
             tc_fence_after();
-            const bool valid = rl < n_rows && debug_in_range(r_abs, 0, p.N, p.status);
-            const int h = g * p.G + hl;
+            const bool valid = rl < n_rows && debug_in_range(r_abs, 0, p.N, p.status) &&
+                               (slot < 0 || debug_in_range(slot, 0, p.n_slots, p.status));
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = p.o + (static_cast<size_t>(r_abs) * p.Hq + h) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tO + c * 32, v);
-                tmem_wait_ld();
-                if (valid) {
-                    uint4 w[4];
-                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        wp[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = w[i];
-                }
-            }
-            if (valid) p.lse[static_cast<size_t>(h) * p.N + r_abs] = (m_used + log2f(l)) * 0.69314718055994531f;
+            const float lse = (m_used + log2f(l)) * 0.69314718055994531f;
+            if (slot < 0)
+                store_o_row<D>(tO, valid, inv, p.o + (static_cast<size_t>(r_abs) * p.Hq + g * p.G + hl) * D,
+                               p.lse + static_cast<size_t>(g * p.G + hl) * p.N + r_abs, lse);
+            else
+                store_partial_row<D>(tO, valid, inv, p, slot, g, m_flat, lse);
         }
     }
 
@@ -341,26 +332,86 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
 }
 
+// Merge of a split block's parts (split-KV; the same rows' softmax over disjoint key sets):
+//   lse = ln sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) O_k
+// with O_k the part's normalised output.  One CTA = one split block x one KV head; warp w takes
+// MMA rows 32w .. 32w + 31 one at a time, its lanes across the head dim.
 template <int D>
-cudaError_t launch_fwd_d(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
-                         cudaStream_t stream, void *const *trace) {
-    const int smem = FwdLayout<D>::bytes;
-    cudaError_t err = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    trace_record(trace, 0, stream);
-    fwd_kernel<D><<<n_blocks * p.Hkv, kThreads, smem, stream>>>(tm_q, kv.k_piece, kv.v_piece, kv.k_half,
-                                                                 kv.v_half, p);
-    err = cudaGetLastError();
-    trace_record(trace, 1, stream);
-    return err;
+__global__ void __launch_bounds__(256) fwd_combine_kernel(const FwdParams p) {
+    constexpr int kPer = D / 32;                      // columns per lane: 2 or 4
+    const int4 cb = __ldg(reinterpret_cast<const int4 *>(p.combine) + blockIdx.x);
+    const int qb = cb.x, slot0 = cb.y, parts = cb.z;
+    const int g = blockIdx.y;
+    const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t lse_base = static_cast<size_t>(p.n_slots) * p.Hkv * 256 * D;
+    for (int m = 32 * warp; m < 32 * warp + 32; ++m) {
+        const int hl = m / p.R, rl = m % p.R;
+        if (rl >= n_rows) continue;                   // warp-uniform
+        const int r_abs = q_row0 + rl, h = g * p.G + hl;
+        if (!debug_in_range(r_abs, 0, p.N, p.status) || !debug_in_range(slot0, 0, p.n_slots, p.status) ||
+            !debug_in_range(slot0 + parts, slot0 + 1, p.n_slots + 1, p.status))
+            continue;
+        float mx = -INFINITY;
+        for (int k = 0; k < parts; ++k)
+            mx = fmaxf(mx, p.partial[lse_base + (static_cast<size_t>(slot0 + k) * p.Hkv + g) * 256 + m]);
+        float acc[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+        float den = 0.f;
+        if (mx > -INFINITY) {
+            for (int k = 0; k < parts; ++k) {
+                const size_t row = (static_cast<size_t>(slot0 + k) * p.Hkv + g) * 256 + m;
+                const float w = expf(p.partial[lse_base + row] - mx);
+                den += w;
+                const float *src = p.partial + row * D + kPer * lane;
+                if constexpr (kPer == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src);
+                    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(src);
+                    acc[0] += w * x.x; acc[1] += w * x.y;
+                }
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        __nv_bfloat16 *dst = p.o + (static_cast<size_t>(r_abs) * p.Hq + h) * D + kPer * lane;
+        if constexpr (kPer == 4) {
+            uint2 w;
+            w.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+            w.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2 *>(dst) = w;
+        } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+        }
+        if (lane == 0) p.lse[static_cast<size_t>(h) * p.N + r_abs] = den > 0.f ? mx + logf(den) : -INFINITY;
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
-                       cudaStream_t stream, void *const *trace) {
-    if (D == 64) return launch_fwd_d<64>(tm_q, kv, p, n_blocks, stream, trace);
-    return launch_fwd_pair(tm_q, kv, p, n_blocks, stream, trace);
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_items,
+                       int n_split, cudaStream_t stream, void *const *trace) {
+    trace_record(trace, 0, stream);
+    cudaError_t err = cudaSuccess;
+    if (D == 64) {
+        constexpr int smem = FwdLayout<64>::bytes;
+        err = cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        fwd_kernel<64><<<n_items * p.Hkv, kThreads, smem, stream>>>(tm_q, kv.k_piece, kv.v_piece, kv.k_half,
+                                                                   kv.v_half, p);
+        err = cudaGetLastError();
+    } else {
+        err = launch_fwd_pair(tm_q, kv, p, n_items, stream);
+    }
+    if (err == cudaSuccess && n_split > 0) {
+        const dim3 grid(n_split, p.Hkv);
+        if (D == 64) fwd_combine_kernel<64><<<grid, 256, 0, stream>>>(p);
+        else fwd_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
+        err = cudaGetLastError();
+    }
+    trace_record(trace, 1, stream);
+    return err;
 }
 
 }  // namespace treeattn

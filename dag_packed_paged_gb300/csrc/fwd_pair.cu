@@ -4,7 +4,8 @@
 // heads of KV head g, O[r,h] = sum_{j in vis(r)} softmax_j(scale q[r,h].k[j,g]) v[j,g] over the
 // key rows the plan's packed tiles list (Octopus arXiv 2611.06956 Section 3.3 Eq. 4 with the
 // rectangular causal alignment after it; HARTS arXiv 2608.28158 Section 4.2 Eq. 21-22) -- with
-// one query block x one KV head per pair of CTAs on neighbouring SMs (a cluster of two).
+// one work item (a query block, or one part of a split block: fwd.cu) x one KV head per pair
+// of CTAs on neighbouring SMs (a cluster of two).
 //
 // The block's 256 MMA rows (R rows x G heads) are split between the two CTAs: CTA r holds query
 // tile r (128 rows) in shared memory and owns the 128 TMEM lanes of those rows.  Every MMA is
@@ -33,6 +34,7 @@
 // O final.
 #include <cfloat>
 
+#include "fwd_store.cuh"
 #include "kernels.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -78,10 +80,10 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool leader = rank == 0;
 
     const int pair = blockIdx.x >> 1;
-    const int qb = __ldg(p.order + pair / p.Hkv);
+    const int4 item = __ldg(reinterpret_cast<const int4 *>(p.items) + pair / p.Hkv);   // work item (fwd.cu)
+    const int qb = item.x, e0 = item.y, E = item.z - item.y, slot = item.w;
     const int g = pair % p.Hkv;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
-    const int e0 = __ldg(p.fblk + 2 * qb), E = __ldg(p.fblk + 2 * qb + 1) - e0;
     const int4 *tiles = reinterpret_cast<const int4 *>(p.ftiles) + 2 * e0;   // two int4 per tile
 
     const uint32_t sQ = sbase + L::q_off, sK = sbase + L::k_off, sV = sbase + L::v_off;
@@ -379,27 +381,16 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_full, 0, abort, p.status));
         if (ok) {
             tc_fence_after();
-            const bool valid = rl < n_rows && debug_in_range(r_abs, 0, p.N, p.status);
+            const bool valid = rl < n_rows && debug_in_range(r_abs, 0, p.N, p.status) &&
+                               (slot < 0 || debug_in_range(slot, 0, p.n_slots, p.status));
             const int hh = g * p.G + hl;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = p.o + (static_cast<size_t>(r_abs) * p.Hq + hh) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tO + c * 32, v);
-                tmem_wait_ld();
-                if (valid) {
-                    uint4 w[4];
-                    uint32_t *wp = reinterpret_cast<uint32_t *>(w);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        wp[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = w[i];
-                }
-            }
-            if (valid) p.lse[static_cast<size_t>(hh) * p.N + r_abs] = (m_used + log2f(l)) * 0.69314718055994531f;
+            const float lse = (m_used + log2f(l)) * 0.69314718055994531f;
+            if (slot < 0)
+                store_o_row<D>(tO, valid, inv, p.o + (static_cast<size_t>(r_abs) * p.Hq + hh) * D,
+                               p.lse + static_cast<size_t>(hh) * p.N + r_abs, lse);
+            else
+                store_partial_row<D>(tO, valid, inv, p, slot, g, m_flat, lse);
         }
     }
 
@@ -414,17 +405,14 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 }  // namespace
 
-cudaError_t launch_fwd_pair(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
-                            cudaStream_t stream, void *const *trace) {
+cudaError_t launch_fwd_pair(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_items,
+                            cudaStream_t stream) {
     const int smem = PairLayout::bytes;
     cudaError_t err = cudaFuncSetAttribute(fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    trace_record(trace, 0, stream);
-    fwd_pair_kernel<<<2 * n_blocks * p.Hkv, kPairThreads, smem, stream>>>(tm_q, kv.k_piece, kv.v_piece, kv.k_half,
-                                                                          kv.v_half, p);
-    err = cudaGetLastError();
-    trace_record(trace, 1, stream);
-    return err;
+    fwd_pair_kernel<<<2 * n_items * p.Hkv, kPairThreads, smem, stream>>>(tm_q, kv.k_piece, kv.v_piece, kv.k_half,
+                                                                         kv.v_half, p);
+    return cudaGetLastError();
 }
 
 }  // namespace treeattn

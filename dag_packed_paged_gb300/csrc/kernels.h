@@ -11,8 +11,10 @@ namespace treeattn {
 struct FwdParams {
     const int32_t *blocks;      // 4 per query block: first row, rows, entry begin, entry end
     const int32_t *ftiles;      // packed key tiles, kPackInts each (plan.h)
-    const int32_t *fblk;        // per query block: first packed tile, end
-    const int32_t *order;       // query blocks, longest first
+    const int32_t *items;       // forward work items, 4 each: block, first tile, end tile, slot (-1: whole block)
+    const int32_t *combine;     // split blocks, 4 each: block, first slot, parts, 0
+    float *partial;             // split parts' O [slots][Hkv][256][D], then lse [slots][Hkv][256]
+    int32_t n_slots;
     const int32_t *page_table;  // logical page -> pool page
     const int32_t *tile_rows;   // per key tile, per page: pool row of the page (TMA y)
     int32_t n_logical_pages;
@@ -89,12 +91,13 @@ struct KvMaps {
     CUtensorMap k_page, v_page, k_piece, v_piece, k_half, v_half;
 };
 
-cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
-                       cudaStream_t stream, void *const *trace);
+// The forward over n_items work items, then (n_split > 0) the combine of the split blocks.
+cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_items,
+                       int n_split, cudaStream_t stream, void *const *trace);
 
 // The forward on CTA pairs (head dim 128; see fwd_pair.cu); launch_fwd dispatches to it.
-cudaError_t launch_fwd_pair(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_blocks,
-                            cudaStream_t stream, void *const *trace);
+cudaError_t launch_fwd_pair(const CUtensorMap &tm_q, const KvMaps &kv, const FwdParams &p, int n_items,
+                            cudaStream_t stream);
 
 cudaError_t launch_bwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const CUtensorMap &tm_do,
                        const BwdParams &p, int n_blocks, int n_chunks, int n_reduce, cudaStream_t stream,

@@ -8,6 +8,7 @@
 // rows sees key j iff j <= h + i).  Instead of materialising Eq. 4's gathered K/V per node,
 // the plan lists the visible compact-row intervals and the kernels read the pages in place.
 #include <algorithm>
+#include <limits>
 #include <array>
 #include <chrono>
 #include <climits>
@@ -513,6 +514,42 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
     const int64_t cap = c.dkdv_chunk_entries > 0 ? int64_t(c.dkdv_chunk_entries)
                                                  : std::max<int64_t>(8, work / (int64_t(P.num_sms) * 4));
     P.chunk_cap = cap;
+
+    // forward work items (split-KV): a query block whose packed-tile list is long against one
+    // worker's average share of the forward is cut into parts of at most fwd_split_cap tiles;
+    // each part is a work item writing a partial O and lse that a combine step merges.  Workers
+    // are SM pairs for head dim 128 (the forward on CTA pairs) and SMs for 64.  Automatic cap:
+    // an eighth of a worker's share of the (block, KV head) tile work, at least 16 tiles.
+    {
+        const int64_t total_tiles = P.fblk_ptr.back() * c.num_kv_heads;
+        const int64_t workers = std::max<int64_t>(1, c.head_dim == 128 ? P.num_sms / 2 : P.num_sms);
+        int64_t split_cap;
+        if (c.fwd_split_tiles < 0) split_cap = std::numeric_limits<int64_t>::max();
+        else if (c.fwd_split_tiles > 0) split_cap = c.fwd_split_tiles;
+        else split_cap = std::max<int64_t>(16, total_tiles / workers / 8);
+        P.fwd_split_cap = split_cap;
+        std::vector<std::array<int32_t, 4>> items;
+        for (int32_t qb : P.fwd_order) {
+            const int64_t a = P.fblk_ptr[qb], z = P.fblk_ptr[qb + 1];
+            if (z - a <= split_cap) {
+                items.push_back({qb, (int32_t)a, (int32_t)z, -1});
+                continue;
+            }
+            // parts of floor or ceil of (z - a) / parts tiles: none empty, none above the cap
+            const int64_t n = z - a, parts = (n + split_cap - 1) / split_cap;
+            P.fwd_combine.insert(P.fwd_combine.end(), {qb, (int32_t)P.n_fwd_slots, (int32_t)parts, 0});
+            for (int64_t k = 0; k < parts; ++k)
+                items.push_back({qb, (int32_t)(a + k * n / parts), (int32_t)(a + (k + 1) * n / parts),
+                                 (int32_t)P.n_fwd_slots++});
+        }
+        // longest first (stable: the block order breaks ties)
+        std::stable_sort(items.begin(), items.end(),
+                         [](const std::array<int32_t, 4> &x, const std::array<int32_t, 4> &y) {
+                             return x[2] - x[1] > y[2] - y[1];
+                         });
+        P.fwd_items.reserve(items.size() * 4);
+        for (auto &it : items) P.fwd_items.insert(P.fwd_items.end(), it.begin(), it.end());
+    }
     std::vector<std::array<int64_t, 4>> ch;
     for (int64_t k = 0; k < n_tiles; ++k) {
         const int64_t a = tptr[k], z = tptr[k + 1];

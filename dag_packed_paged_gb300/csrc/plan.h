@@ -68,6 +68,12 @@ struct HostPlan {
     std::vector<int32_t> t_info;      // per tile-major entry: block << 2 | flags, first row, lo, hi
     std::vector<int32_t> ftiles;      // packed key tiles of the query-major kernels (kPackInts each)
     std::vector<int64_t> fblk_ptr;    // n_blocks + 1: block b's packed tiles [fblk_ptr[b], fblk_ptr[b+1])
+    // forward work items (split-KV): 4 per item, longest first: block, first packed tile, end
+    // tile, partial slot (-1: the item is the whole block and writes O and lse itself)
+    std::vector<int32_t> fwd_items;
+    std::vector<int32_t> fwd_combine; // 4 per split block: block, first slot, parts, 0
+    int64_t n_fwd_slots = 0;          // partial results of split blocks (one per part)
+    int64_t fwd_split_cap = 0;        // packed tiles per forward item at most
     int64_t n_segments = 0;
     int64_t n_partial_slots = 0;
     int64_t chunk_cap = 0;            // entries per dK/dV chunk at most
@@ -100,6 +106,9 @@ struct ta_plan {
     const int32_t *d_page_table = nullptr;
     const int32_t *d_tile_rows = nullptr;
     const int32_t *d_t_info = nullptr;
+    const int32_t *d_fwd_items = nullptr;
+    const int32_t *d_fwd_combine = nullptr;
+    float *d_fwd_partial = nullptr;   // [slots][Hkv][256][D] O then [slots][Hkv][256] lse (own allocation)
     const int32_t *d_pos_ids = nullptr;   // Eq. 2 position of every compact row
     const int32_t *d_ftiles = nullptr;    // packed key tiles (forward, dQ)
     const int32_t *d_fblk = nullptr;      // per block: first packed tile, end (2 x int32)

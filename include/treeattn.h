@@ -108,7 +108,16 @@ typedef struct {
  * key tile) entries, each chunk one CTA, whose partial sums a fixed-order reduction adds.
  * dkdv_chunk_entries <= 0 selects max(8, entries * num_kv_heads / (4 * SMs)): no chunk longer
  * than about a quarter of an SM's average share.  SMs = num_sms if > 0, else the SM count of
- * the current device (152 on GB300) -- or 152 for a TA_PLAN_HOST_ONLY plan, which has no device. */
+ * the current device (152 on GB300) -- or 152 for a TA_PLAN_HOST_ONLY plan, which has no device.
+ *
+ * Split-KV forward (results equal up to fp32 summation order): a query block whose list of
+ * packed key tiles is longer than fwd_split_tiles is cut into parts of at most that many tiles;
+ * each part runs as its own work item and writes a partial O and lse to plan-owned device
+ * memory, and a combine kernel merges the parts of each split block (O = sum_k w_k O_k with
+ * w_k = exp(lse_k - lse), lse = ln sum_k exp(lse_k)).  fwd_split_tiles == 0 selects an eighth
+ * of one worker's average share of the forward's tile work (workers: SM pairs for head_dim 128,
+ * SMs for 64), at least 16; < 0 never splits.  Forwards of a plan that has split blocks share
+ * its partial buffer: such forwards must not run at the same time on different streams. */
 typedef struct {
     int32_t num_q_heads;
     int32_t num_kv_heads;
@@ -119,6 +128,7 @@ typedef struct {
     int64_t num_pages;
     int32_t num_sms;             /* 0: the device's (see above) */
     int32_t dkdv_chunk_entries;  /* 0: derived from the SM count (see above) */
+    int32_t fwd_split_tiles;     /* 0: automatic, < 0: never (see above) */
 } ta_config;
 
 typedef struct ta_plan ta_plan; /* opaque; owned by the library */
@@ -144,6 +154,9 @@ typedef struct {
     int64_t chunk_cap;       /* entries per dK/dV chunk at most (see ta_config) */
     int32_t num_sms;         /* SM count the chunk cap was derived from */
     int32_t device;          /* CUDA device the plan was uploaded to (-1: host-only plan) */
+    int64_t n_fwd_items;     /* forward work items (blocks, or parts of split blocks) */
+    int64_t n_fwd_split;     /* query blocks whose forward is split into parts */
+    int64_t fwd_split_cap;   /* packed key tiles per forward work item at most */
 } ta_plan_stats;
 
 /* Host views of the plan's arrays, for inspection and bit-exact tests.  All pointers are
@@ -166,6 +179,9 @@ typedef struct {
  *                                      visible rows [lo, hi) of the piece), flags, 0}; flags bit
  *                                      0 = some slot needs masking, bit 1+k = slot k causal
  *                                      (mask j > r), bit 5+h = slots 2h, 2h+1 are one 64-row run
+ *   fwd_items[4*n_fwd_items]           forward work items in launch order: {block, first packed
+ *                                      tile, end tile, partial slot or -1 (whole block)}
+ *   fwd_combine[4*n_fwd_split]         split blocks: {block, first slot, parts, 0}
  * flags (entries): bit 0 = causal (mask j > r), bit 1 = the entry does not cover its whole tile. */
 typedef struct {
     int64_t n_rows, n_blocks, n_intervals, n_entries, n_chunks;
@@ -181,6 +197,9 @@ typedef struct {
     int64_t n_ftiles;
     const int64_t *fblk_ptr;
     const int32_t *ftiles;
+    int64_t n_fwd_items, n_fwd_split;
+    const int32_t *fwd_items;
+    const int32_t *fwd_combine;
 } ta_plan_arrays;
 
 /* Build the compact prefix-tree episode of a set of token trajectories.

@@ -410,3 +410,76 @@ def test_chunk_cap_override_gives_unsplit_long_chunks():
     # the chunking changes nothing else in the plan
     for key in ("blocks", "entries", "t_entries"):
         assert np.array_equal(ex[key], ex1[key])
+
+
+def _check_fwd_items(st, ex, cap):
+    """The forward's work items cover each query block's packed tiles exactly once, in parts of
+    at most `cap` tiles, longest first; split blocks' parts own consecutive partial slots."""
+    items, comb, fblk = ex["fwd_items"], ex["fwd_combine"], ex["fblk_ptr"]
+    nb = len(fblk) - 1
+    assert st["n_fwd_items"] == len(items) and st["n_fwd_split"] == len(comb)
+    lens = items[:, 2] - items[:, 1]
+    assert (lens >= 1).all() and (lens <= cap).all()
+    assert (np.diff(lens) <= 0).all()                        # longest first
+    seen = np.zeros(int(fblk[-1]), dtype=np.int32)
+    for b, a, z, slot in items:
+        assert fblk[b] <= a < z <= fblk[b + 1]
+        seen[a:z] += 1
+    assert (seen == 1).all()
+    split = {int(c[0]): c for c in comb}
+    slots = []
+    for b in range(nb):
+        mine = items[items[:, 0] == b]
+        if b in split:
+            _, s0, parts, zero = split[b]
+            assert zero == 0 and len(mine) == parts >= 2
+            assert sorted(mine[:, 3].tolist()) == list(range(s0, s0 + parts))
+            # slot order follows the tiles
+            by_slot = mine[np.argsort(mine[:, 3])]
+            assert (by_slot[1:, 1] == by_slot[:-1, 2]).all()
+            slots += by_slot[:, 3].tolist()
+        else:
+            assert len(mine) == 1 and mine[0, 3] == -1
+            assert (mine[0, 1], mine[0, 2]) == (fblk[b], fblk[b + 1])
+    assert sorted(slots) == list(range(len(slots)))
+
+
+@pytest.mark.parametrize("cap", [1, 3, 7])
+def test_fwd_split_items_cover_every_tile_once(cap):
+    """fwd_split_tiles forces split-KV: every block longer than the cap becomes parts of at most
+    cap tiles, nothing is visited twice, and the rest of the plan is unchanged."""
+    ep = W.Episode(name="chain", branches=W.make_branches([-1, 0, 0], [0, 700, 1500], [2048, 600, 900]),
+                   mounts=W.make_mounts([]), num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=64)
+    forced = host_plan(ep, fwd_split_tiles=cap)
+    st, ex = ta.tree_attn_plan_stats(forced), ta.tree_attn_plan_export(forced)
+    assert st["fwd_split_cap"] == cap
+    _check_fwd_items(st, ex, cap)
+    lens = np.diff(ex["fblk_ptr"])
+    assert st["n_fwd_split"] == int((lens > cap).sum()) > 0
+    assert st["n_fwd_items"] == int(np.where(lens > cap, -(-lens // cap), 1).sum())
+    whole = host_plan(ep, fwd_split_tiles=-1)
+    stw, exw = ta.tree_attn_plan_stats(whole), ta.tree_attn_plan_export(whole)
+    assert stw["n_fwd_split"] == 0 and stw["n_fwd_items"] == len(lens)
+    _check_fwd_items(stw, exw, int(lens.max()))
+    for key in ("blocks", "entries", "t_entries", "chunks", "ftiles", "fblk_ptr", "fwd_order"):
+        assert np.array_equal(ex[key], exw[key]), key
+
+
+def test_fwd_split_auto_keeps_ordinary_blocks_whole():
+    """The automatic cap (an eighth of one worker's share of the tile work, at least 16) splits
+    nothing on a workload of many comparable blocks, and splits the one long block of a
+    workload that is mostly that block."""
+    ep = W.wide_fan()
+    st = ta.tree_attn_plan_stats(host_plan(ep, num_sms=152))
+    assert st["n_fwd_split"] == 0 and st["n_fwd_items"] == st["n_blocks"]
+    # a single causal chain of 128 query blocks (fewer items than SMs): its later blocks are
+    # longer than 16 tiles, which is above an eighth of a worker's share of the work
+    chain = W.Episode(name="chain", branches=W.make_branches([-1], [0], [8192]), mounts=W.make_mounts([]),
+                      num_q_heads=4, num_kv_heads=1, head_dim=64, page_size=64)
+    p = host_plan(chain, num_sms=152)
+    st, ex = ta.tree_attn_plan_stats(p), ta.tree_attn_plan_export(p)
+    lens = np.diff(ex["fblk_ptr"])
+    share = lens.sum() / 152
+    assert st["fwd_split_cap"] == max(16, int(share // 8))
+    assert st["n_fwd_split"] > 0
+    _check_fwd_items(st, ex, st["fwd_split_cap"])
