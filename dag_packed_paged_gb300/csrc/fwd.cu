@@ -334,8 +334,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 // Merge of a split block's parts (split-KV; the same rows' softmax over disjoint key sets):
 //   lse = ln sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) O_k
-// with O_k the part's normalised output.  One CTA = one split block x one KV head; warp w takes
-// MMA rows 32w .. 32w + 31 one at a time, its lanes across the head dim.
+// with O_k the part's normalised output.  Grid (split blocks, KV heads, 8): a CTA takes 32 of
+// the block's 256 MMA rows, a warp 4 of them.  Per row the lanes first run across the parts
+// (max and sum of exp(lse_k - max)), then across the head dim, with the parts' loads unrolled
+// so that several are in flight: the kernel is bound by the latency of those loads, not by
+// their bytes (each part is read once).
 template <int D>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const FwdParams p) {
     constexpr int kPer = D / 32;                      // columns per lane: 2 or 4
@@ -344,32 +347,40 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const FwdParams p) {
     const int g = blockIdx.y;
     const int q_row0 = __ldg(p.blocks + 4 * qb), n_rows = __ldg(p.blocks + 4 * qb + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t lse_base = static_cast<size_t>(p.n_slots) * p.Hkv * 256 * D;
-    for (int m = 32 * warp; m < 32 * warp + 32; ++m) {
+    if (!debug_in_range(slot0, 0, p.n_slots, p.status) || !debug_in_range(slot0 + parts, slot0 + 1, p.n_slots + 1, p.status))
+        return;
+    const size_t stride = static_cast<size_t>(p.Hkv) * 256;          // rows between consecutive slots
+    const float *lse_part = p.partial + static_cast<size_t>(p.n_slots) * stride * D +
+                            (static_cast<size_t>(slot0) * p.Hkv + g) * 256;
+    const float *o_part = p.partial + (static_cast<size_t>(slot0) * p.Hkv + g) * 256 * D + kPer * lane;
+    for (int i = 0; i < 4; ++i) {
+        const int m = 32 * blockIdx.z + 4 * warp + i;
         const int hl = m / p.R, rl = m % p.R;
         if (rl >= n_rows) continue;                   // warp-uniform
         const int r_abs = q_row0 + rl, h = g * p.G + hl;
-        if (!debug_in_range(r_abs, 0, p.N, p.status) || !debug_in_range(slot0, 0, p.n_slots, p.status) ||
-            !debug_in_range(slot0 + parts, slot0 + 1, p.n_slots + 1, p.status))
-            continue;
+        if (!debug_in_range(r_abs, 0, p.N, p.status)) continue;
         float mx = -INFINITY;
-        for (int k = 0; k < parts; ++k)
-            mx = fmaxf(mx, p.partial[lse_base + (static_cast<size_t>(slot0 + k) * p.Hkv + g) * 256 + m]);
+        for (int k = lane; k < parts; k += 32) mx = fmaxf(mx, __ldcg(lse_part + k * stride + m));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float den = 0.f;
+        if (mx > -INFINITY)
+            for (int k = lane; k < parts; k += 32) den += expf(__ldcg(lse_part + k * stride + m) - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         float acc[kPer];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-        float den = 0.f;
+        for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
         if (mx > -INFINITY) {
+#pragma unroll 4
             for (int k = 0; k < parts; ++k) {
-                const size_t row = (static_cast<size_t>(slot0 + k) * p.Hkv + g) * 256 + m;
-                const float w = expf(p.partial[lse_base + row] - mx);
-                den += w;
-                const float *src = p.partial + row * D + kPer * lane;
+                const float w = expf(__ldcg(lse_part + k * stride + m) - mx);
+                const float *src = o_part + (k * stride + m) * D;
                 if constexpr (kPer == 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(src);
+                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
                     acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
                 } else {
-                    const float2 x = *reinterpret_cast<const float2 *>(src);
+                    const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
                     acc[0] += w * x.x; acc[1] += w * x.y;
                 }
             }
@@ -405,7 +416,7 @@ cudaError_t launch_fwd(int D, const CUtensorMap &tm_q, const KvMaps &kv, const F
         err = launch_fwd_pair(tm_q, kv, p, n_items, stream);
     }
     if (err == cudaSuccess && n_split > 0) {
-        const dim3 grid(n_split, p.Hkv);
+        const dim3 grid(n_split, p.Hkv, 8);
         if (D == 64) fwd_combine_kernel<64><<<grid, 256, 0, stream>>>(p);
         else fwd_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
         err = cudaGetLastError();

@@ -8,7 +8,6 @@
 // rows sees key j iff j <= h + i).  Instead of materialising Eq. 4's gathered K/V per node,
 // the plan lists the visible compact-row intervals and the kernels read the pages in place.
 #include <algorithm>
-#include <limits>
 #include <array>
 #include <chrono>
 #include <climits>
@@ -516,17 +515,22 @@ int build_host_plan(const ta_branch *branches, int32_t n_branches, const ta_moun
     P.chunk_cap = cap;
 
     // forward work items (split-KV): a query block whose packed-tile list is long against one
-    // worker's average share of the forward is cut into parts of at most fwd_split_cap tiles;
-    // each part is a work item writing a partial O and lse that a combine step merges.  Workers
-    // are SM pairs for head dim 128 (the forward on CTA pairs) and SMs for 64.  Automatic cap:
-    // an eighth of a worker's share of the (block, KV head) tile work, at least 16 tiles.
+    // worker's share of the forward is cut into parts of at most fwd_split_cap tiles; each part
+    // is a work item writing a partial O and lse that a combine step merges.  Workers are SM
+    // pairs for head dim 128 (the forward on CTA pairs) and SMs for 64.  The (block, KV head)
+    // items run longest first, so the forward's span is about max(share, longest block): only
+    // a longest block well above the share (1.5x, and by 32 tiles: the combine and the parts'
+    // partial O cost about as much as 8 tiles) is worth splitting, and then the automatic cap
+    // is the share (at least 16 tiles).  Otherwise the cap is the longest block (no split).
     {
-        const int64_t total_tiles = P.fblk_ptr.back() * c.num_kv_heads;
+        int64_t longest = 0;
+        for (size_t b = 0; b + 1 < P.fblk_ptr.size(); ++b) longest = std::max(longest, P.fblk_ptr[b + 1] - P.fblk_ptr[b]);
         const int64_t workers = std::max<int64_t>(1, c.head_dim == 128 ? P.num_sms / 2 : P.num_sms);
-        int64_t split_cap;
-        if (c.fwd_split_tiles < 0) split_cap = std::numeric_limits<int64_t>::max();
-        else if (c.fwd_split_tiles > 0) split_cap = c.fwd_split_tiles;
-        else split_cap = std::max<int64_t>(16, total_tiles / workers / 8);
+        const int64_t share = (P.fblk_ptr.back() * c.num_kv_heads + workers - 1) / workers;
+        int64_t split_cap = longest;
+        if (c.fwd_split_tiles > 0) split_cap = c.fwd_split_tiles;
+        else if (c.fwd_split_tiles == 0 && 2 * longest > 3 * share && longest - share >= 32)
+            split_cap = std::max<int64_t>(16, share);
         P.fwd_split_cap = split_cap;
         std::vector<std::array<int32_t, 4>> items;
         for (int32_t qb : P.fwd_order) {

@@ -114,10 +114,13 @@ typedef struct {
  * packed key tiles is longer than fwd_split_tiles is cut into parts of at most that many tiles;
  * each part runs as its own work item and writes a partial O and lse to plan-owned device
  * memory, and a combine kernel merges the parts of each split block (O = sum_k w_k O_k with
- * w_k = exp(lse_k - lse), lse = ln sum_k exp(lse_k)).  fwd_split_tiles == 0 selects an eighth
- * of one worker's average share of the forward's tile work (workers: SM pairs for head_dim 128,
- * SMs for 64), at least 16; < 0 never splits.  Forwards of a plan that has split blocks share
- * its partial buffer: such forwards must not run at the same time on different streams. */
+ * w_k = exp(lse_k - lse), lse = ln sum_k exp(lse_k)).  fwd_split_tiles == 0 (automatic)
+ * splits only when the longest block is more than 1.5x, and at least 32 tiles above, one
+ * worker's share of the forward's tile work (share = packed tiles x num_kv_heads / workers;
+ * workers: SM pairs for head_dim 128, SMs for 64), and then into parts of at most
+ * max(16, share) tiles; < 0 never splits.
+ * Forwards of a plan that has split blocks share its partial buffer: such forwards must not
+ * run at the same time on different streams. */
 typedef struct {
     int32_t num_q_heads;
     int32_t num_kv_heads;
@@ -156,7 +159,8 @@ typedef struct {
     int32_t device;          /* CUDA device the plan was uploaded to (-1: host-only plan) */
     int64_t n_fwd_items;     /* forward work items (blocks, or parts of split blocks) */
     int64_t n_fwd_split;     /* query blocks whose forward is split into parts */
-    int64_t fwd_split_cap;   /* packed key tiles per forward work item at most */
+    int64_t fwd_split_cap;   /* packed key tiles per forward work item at most (the longest
+                                block's when nothing is split) */
 } ta_plan_stats;
 
 /* Host views of the plan's arrays, for inspection and bit-exact tests.  All pointers are

@@ -465,21 +465,28 @@ def test_fwd_split_items_cover_every_tile_once(cap):
         assert np.array_equal(ex[key], exw[key]), key
 
 
-def test_fwd_split_auto_keeps_ordinary_blocks_whole():
-    """The automatic cap (an eighth of one worker's share of the tile work, at least 16) splits
-    nothing on a workload of many comparable blocks, and splits the one long block of a
-    workload that is mostly that block."""
+def test_fwd_split_auto_only_when_the_longest_block_dominates():
+    """The automatic cap splits only when the longest block exceeds 1.5x one worker's share of
+    the tile work and by at least 32 tiles (workers: SMs for head dim 64, SM pairs for 128),
+    into parts of at most max(16, share) tiles; otherwise it keeps every block whole."""
+    def chain(n, d, heads):
+        return W.Episode(name="chain", branches=W.make_branches([-1], [0], [n]), mounts=W.make_mounts([]),
+                         num_q_heads=heads[0], num_kv_heads=heads[1], head_dim=d, page_size=64)
+
     ep = W.wide_fan()
     st = ta.tree_attn_plan_stats(host_plan(ep, num_sms=152))
     assert st["n_fwd_split"] == 0 and st["n_fwd_items"] == st["n_blocks"]
-    # a single causal chain of 128 query blocks (fewer items than SMs): its later blocks are
-    # longer than 16 tiles, which is above an eighth of a worker's share of the work
-    chain = W.Episode(name="chain", branches=W.make_branches([-1], [0], [8192]), mounts=W.make_mounts([]),
-                      num_q_heads=4, num_kv_heads=1, head_dim=64, page_size=64)
-    p = host_plan(chain, num_sms=152)
-    st, ex = ta.tree_attn_plan_stats(p), ta.tree_attn_plan_export(p)
-    lens = np.diff(ex["fblk_ptr"])
-    share = lens.sum() / 152
-    assert st["fwd_split_cap"] == max(16, int(share // 8))
-    assert st["n_fwd_split"] > 0
-    _check_fwd_items(st, ex, st["fwd_split_cap"])
+    cases = [(8192, 64, (4, 1), True), (16384, 128, (1, 1), True), (4096, 128, (4, 1), False),
+             (16384, 128, (4, 1), False), (8192, 128, (16, 4), False)]
+    for n, d, heads, splits in cases:
+        p = host_plan(chain(n, d, heads), num_sms=152)
+        st, ex = ta.tree_attn_plan_stats(p), ta.tree_attn_plan_export(p)
+        lens = np.diff(ex["fblk_ptr"])
+        workers = 152 if d == 64 else 76
+        share = -(-int(lens.sum()) * heads[1] // workers)
+        assert (2 * lens.max() > 3 * share and lens.max() - share >= 32) == splits, (n, d, heads)
+        if splits:
+            assert st["fwd_split_cap"] == max(16, share) and st["n_fwd_split"] > 0
+        else:
+            assert st["fwd_split_cap"] == lens.max() and st["n_fwd_split"] == 0
+        _check_fwd_items(st, ex, st["fwd_split_cap"])
