@@ -572,27 +572,40 @@ def main():
 
     # ---------------------------------------------------------------- end to end, host buffers
     # Every step plans its episode on the host, copies its inputs from pinned host memory and
-    # reads every output back.  Steps are pipelined the way a training loop feeds a GPU: two
-    # sets of device buffers alternate, the copies run on their own streams, and plans are
-    # built and freed in stream order (TA_PLAN_STREAM_ORDERED), so step i's planning and
-    # copies overlap the attention of steps i-1 and i+1.  The timed region starts before the
-    # first step's planning and ends after the last step's outputs are on the host.
+    # reads every output back.  Steps are pipelined the way a training loop feeds a GPU: four
+    # sets of device buffers rotate, the copies run on their own streams, and plans are built
+    # and freed in stream order (TA_PLAN_STREAM_ORDERED).  Step i's input copy is issued before
+    # its host planning and overlaps the attention of steps i-1 and i-2 (dO last: only the
+    # backward needs it); O and lse are read back while the backward runs, dQ while the dK/dV
+    # kernel runs (the plan's trace event after the dQ kernel), dK/dV at the end.  With four
+    # buffer sets each copy has three steps of compute to finish in: a host<->device copy can
+    # run several times slower than its usual rate while other processes load the host's
+    # memory, which with two sets would leave the GPU idle.  The
+    # timed region starts before the first step's copy and planning and ends after the last
+    # step's outputs are on the host.
     e2e = None
     if not args.no_e2e:
+        NB = 4
         h_in = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in (t.q, pool.k_pool, pool.v_pool, t.do)]
-        d_in = [[q, k_pool, v_pool, d_o], [torch.empty_like(x) for x in (q, k_pool, v_pool, d_o)]]
-        d_out = [[o, lse, dq, dk_pool, dv_pool], [torch.empty_like(x) for x in (o, lse, dq, dk_pool, dv_pool)]]
-        h_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in d_out[0]] for _ in range(2)]
+        d_in = [[q, k_pool, v_pool, d_o]] + [[torch.empty_like(x) for x in (q, k_pool, v_pool, d_o)]
+                                             for _ in range(NB - 1)]
+        d_out = [[o, lse, dq, dk_pool, dv_pool]] + [[torch.empty_like(x) for x in (o, lse, dq, dk_pool, dv_pool)]
+                                                    for _ in range(NB - 1)]
+        h_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in d_out[0]] for _ in range(NB)]
         h2d = sum(h.numel() * h.element_size() for h in h_in)
         d2h = sum(h.numel() * h.element_size() for h in h_out[0])
         comp_s, h2d_s, d2h_s = (torch.cuda.Stream(dev) for _ in range(3))
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        comp_done = [torch.cuda.Event() for _ in range(2)]
-        out_read = [torch.cuda.Event() for _ in range(2)]
-        for b in range(2):                      # mark both buffer sets free
+        in_fwd = [torch.cuda.Event() for _ in range(NB)]
+        in_ready = [torch.cuda.Event() for _ in range(NB)]
+        fwd_done = [torch.cuda.Event() for _ in range(NB)]
+        dq_done = [torch.cuda.Event() for _ in range(NB)]
+        comp_done = [torch.cuda.Event() for _ in range(NB)]
+        out_read = [torch.cuda.Event() for _ in range(NB)]
+        for b in range(NB):                     # mark every buffer set free
             comp_done[b].record(comp_s)
             out_read[b].record(d2h_s)
-        e2e_steps = max(3, K)                  # the same step count as the device-resident loop
+            dq_done[b].record(comp_s)           # creates the event the library records
+        e2e_steps = max(20, K)
 
         def plan_async():
             return ta.tree_attn_plan(ep.branches, ep.mounts, pool.page_table, num_q_heads=Hq,
@@ -601,28 +614,34 @@ def main():
                                      stream=comp_s)
 
         def e2e_step(i):
-            b = i % 2
-            p2 = plan_async()                                 # host planner; upload ordered on comp_s
-            h2d_s.wait_event(comp_done[b])                    # step i-2 has finished reading set b
+            b = i % NB
+            h2d_s.wait_event(comp_done[b])                    # step i-NB has finished reading set b
             with torch.cuda.stream(h2d_s):
-                for dv_, hv in zip(d_in[b], h_in):
+                for dv_, hv in zip(d_in[b][:3], h_in[:3]):   # q, k_pool, v_pool
                     dv_.view(torch.int16).copy_(hv, non_blocking=True)
+                in_fwd[b].record(h2d_s)
+                d_in[b][3].view(torch.int16).copy_(h_in[3], non_blocking=True)
             in_ready[b].record(h2d_s)
-            comp_s.wait_event(in_ready[b])
-            comp_s.wait_event(out_read[b])                    # step i-2's outputs are on the host
+            p2 = plan_async()                                 # host planner; upload ordered on comp_s
+            ta.tree_attn_set_trace_events(p2, [None, None, None, None, dq_done[b], None, None])
+            comp_s.wait_event(in_fwd[b])
+            comp_s.wait_event(out_read[b])                    # step i-NB's outputs are on the host
             qq, kk, vv, dd = d_in[b]
             oo, ll, gq, gk, gv = d_out[b]
             ta.tree_attn_fwd(p2, qq, kk, vv, oo, ll, stream=comp_s)
+            fwd_done[b].record(comp_s)
+            comp_s.wait_event(in_ready[b])
             ta.tree_attn_bwd(p2, qq, kk, vv, oo, ll, dd, gq, gk, gv, ws, stream=comp_s)
             comp_done[b].record(comp_s)
-            d2h_s.wait_event(comp_done[b])
-            with torch.cuda.stream(d2h_s):
-                for dv_, hv in zip(d_out[b], h_out[b]):
-                    hv.copy_(dv_, non_blocking=True)
+            for ready, idx in ((fwd_done[b], (0, 1)), (dq_done[b], (2,)), (comp_done[b], (3, 4))):
+                d2h_s.wait_event(ready)                       # O, lse | dQ | dK, dV
+                with torch.cuda.stream(d2h_s):
+                    for k_ in idx:
+                        h_out[b][k_].copy_(d_out[b][k_], non_blocking=True)
             out_read[b].record(d2h_s)
             return p2
 
-        for i in range(2):                                    # untimed: one use of each buffer set
+        for i in range(NB):                                   # untimed: one use of each buffer set
             keep = e2e_step(i)
         torch.cuda.synchronize(dev)
         ta.tree_attn_check(keep, comp_s)
@@ -635,7 +654,7 @@ def main():
         plans = []
         for i in range(e2e_steps):
             plans.append(e2e_step(i))
-            if len(plans) > 2:
+            if len(plans) > NB:
                 plans.pop(0)                                  # freed in comp_s order, after its use
         comp_s.wait_stream(d2h_s)
         comp_s.wait_stream(h2d_s)
@@ -647,8 +666,9 @@ def main():
         e2e = {"value": (flops_fwd + flops_bwd) * world / e2e_ms / 1e9, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                "steps": e2e_steps, "includes": "per step: plan + H2D of q/k_pool/v_pool/dO from pinned host + fwd "
-                                               "+ bwd + D2H of o/lse/dq/dk_pool/dv_pool; steps pipelined over two "
-                                               "buffer sets and three streams"}
+                                               "+ bwd + D2H of o/lse/dq/dk_pool/dv_pool; steps pipelined over four "
+                                               "buffer sets and three streams; pipeline fill and drain inside the "
+                                               "timed region"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,

@@ -498,7 +498,8 @@ int tree_attn_check(const ta_plan *plan, void *stream);
 int tree_attn_selftest_timeout(const ta_plan *plan, int64_t limit_us, void *stream);
 
 /* Optional per-kernel tracing.  With events set, tree_attn_fwd records events[0] before and
- * events[1] after its kernel; tree_attn_bwd records events[2], [3], [4], [5] before its
+ * events[1] after its kernels (the forward and, for a plan with split blocks, the combine);
+ * tree_attn_bwd records events[2], [3], [4], [5] before its
  * delta, dQ, dK/dV and reduce kernels and events[6] after the last one -- all on the call's
  * stream (cudaEvent_t handles created and owned by the caller; entries may be NULL).  Pass
  * events = NULL to stop.  n_events must be 7 unless events is NULL. */
