@@ -72,3 +72,29 @@ def test_forced_split_small_pages(page):
     run = Run(ep, dist="sharp", fwd_split_tiles=2)
     assert ta.tree_attn_plan_stats(run.plan)["n_fwd_split"] > 0
     _check(run, ep, bwd=False)
+
+
+def test_split_forward_in_a_graph_and_stream_ordered():
+    """A plan with split blocks: the forward (work items and combine) captured in a CUDA graph
+    replays bit-identically, and a stream-ordered plan (its partial buffer allocated in stream
+    order) gives the same O and lse as the ordinary plan, bit for bit."""
+    import torch
+    ep = W.random_small(4300, max_branches=8, max_len=900, heads=(8, 2), head_dim=128, page_size=64, n_mounts=3)
+    run = Run(ep, dist="realistic", fwd_split_tiles=2)
+    assert ta.tree_attn_plan_stats(run.plan)["n_fwd_split"] > 0
+    o, lse = run.fwd()
+    eager_o, eager_lse = run.o.clone(), run.lse.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ta.tree_attn_fwd(run.plan, run.q, run.k_pool, run.v_pool, run.o, run.lse)
+    for _ in range(2):
+        run.o.fill_(float("nan"))
+        run.lse.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ta.tree_attn_check(run.plan)
+        assert torch.equal(run.o.view(torch.int16), eager_o.view(torch.int16))
+        assert torch.equal(run.lse.view(torch.int32), eager_lse.view(torch.int32))
+    so = Run(ep, tensors=run.t, pool=run.pool, flags=ta.TA_PLAN_STREAM_ORDERED, fwd_split_tiles=2)
+    o2, lse2 = so.fwd()
+    assert np.array_equal(o2, o) and np.array_equal(lse2, lse)
