@@ -31,10 +31,16 @@ def episodes():
                                              page_size=16, n_mounts=2)
     yield "random D=128 P=128", W.random_small(2002, max_branches=8, max_len=700, heads=(8, 1), head_dim=128,
                                                page_size=128, n_mounts=3)
+    # split-KV forward: work items over parts of blocks, partial slots and the combine (checked
+    # slot indexes), on both forwards
+    yield "split D=128 cap 2", W.random_small(2003, max_branches=8, max_len=900, heads=(8, 2), head_dim=128,
+                                              page_size=64, n_mounts=3)
+    yield "split D=64 cap 2", W.random_small(2004, max_branches=8, max_len=900, heads=(8, 2), head_dim=64,
+                                             page_size=32, n_mounts=3)
 
 
 for name, ep in episodes():
-    run = Run(ep)
+    run = Run(ep, fwd_split_tiles=2) if name.startswith("split") else Run(ep)
     o, lse = run.fwd()                 # tree_attn_check raises on a bounds flag
     dq, dk, dv = run.bwd()
     ref = oracle.run(ep.branches, ep.mounts, run.t.q, run.t.k, run.t.v, run.t.do, ep.softmax_scale)

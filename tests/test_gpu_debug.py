@@ -19,4 +19,4 @@ def test_debug_build_matches_oracle_without_bounds_flags():
     r = subprocess.run([sys.executable, os.path.join(HERE, "debug_child.py")], env=env, capture_output=True,
                        text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert r.stdout.count("no bounds flag") == 5, r.stdout
+    assert r.stdout.count("no bounds flag") == 7, r.stdout
