@@ -610,9 +610,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             ky[i] = i < ppt ? __ldg(p.tile_rows + tile * ppt + i) : 0;
-            // (TA_DEBUG) a pool row outside the pool reads the zero-filled row past it instead
-            if (!debug_in_range(ky[i], 0, static_cast<long long>(p.num_pages) * p.page_size, p.status))
-                ky[i] = p.num_pages * p.page_size;
+            // (TA_DEBUG) a page of the tile past the strip's end has the row one past the pool,
+            // which TMA zero-fills; any other row outside the pool is flagged and replaced by it
+            const long long past = static_cast<long long>(p.num_pages) * p.page_size;
+            if (!debug_in_range(ky[i], 0, past + 1, p.status)) ky[i] = static_cast<int>(past);
         }
         if (lane == 0) {
             tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
