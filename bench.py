@@ -574,9 +574,9 @@ def main():
     # Every step plans its episode on the host, copies its inputs from pinned host memory and
     # reads every output back.  Steps are pipelined the way a training loop feeds a GPU: four
     # sets of device buffers rotate, the copies run on their own streams, and plans are built
-    # and freed in stream order (TA_PLAN_STREAM_ORDERED).  Step i's input copy is issued before
-    # its host planning and overlaps the attention of steps i-1 and i-2 (dO last: only the
-    # backward needs it); O and lse are read back while the backward runs, dQ while the dK/dV
+    # and freed in stream order (TA_PLAN_STREAM_ORDERED), each one step ahead of its use.  Step
+    # i's input copy overlaps the attention of the steps before it (dO last: only the backward
+    # needs it); O and lse are read back while the backward runs, dQ while the dK/dV
     # kernel runs (the plan's trace event after the dQ kernel), dK/dV at the end.  With four
     # buffer sets each copy has three steps of compute to finish in: a host<->device copy can
     # run several times slower than its usual rate while other processes load the host's
@@ -613,7 +613,12 @@ def main():
                                      num_pages=pool.k_pool.shape[0], flags=ta.TA_PLAN_STREAM_ORDERED,
                                      stream=comp_s)
 
-        def e2e_step(i):
+        def e2e_step(i, p2, last):
+            """Step i on buffer set i mod NB with its plan p2, built during step i-1 (None for the
+            first step, which plans while its inputs are copied).  Returns (p2, step i+1's plan):
+            the next plan is built once step i's kernels and copies are queued, so that its
+            upload has a whole step to finish in (a copy engine busy with the large input
+            copies can hold a small upload back for tens of ms); None after the last step."""
             b = i % NB
             h2d_s.wait_event(comp_done[b])                    # step i-NB has finished reading set b
             with torch.cuda.stream(h2d_s):
@@ -622,7 +627,8 @@ def main():
                 in_fwd[b].record(h2d_s)
                 d_in[b][3].view(torch.int16).copy_(h_in[3], non_blocking=True)
             in_ready[b].record(h2d_s)
-            p2 = plan_async()                                 # host planner; upload ordered on comp_s
+            if p2 is None:
+                p2 = plan_async()
             ta.tree_attn_set_trace_events(p2, [None, None, None, None, dq_done[b], None, None])
             comp_s.wait_event(in_fwd[b])
             comp_s.wait_event(out_read[b])                    # step i-NB's outputs are on the host
@@ -639,21 +645,25 @@ def main():
                     for k_ in idx:
                         h_out[b][k_].copy_(d_out[b][k_], non_blocking=True)
             out_read[b].record(d2h_s)
-            return p2
+            return p2, (None if last else plan_async())      # host planner; upload ordered on comp_s
 
-        for i in range(NB):                                   # untimed: one use of each buffer set
-            keep = e2e_step(i)
+        warm, nxt = [], None                                  # untimed: one use of each buffer set
+        for i in range(NB):
+            cur, nxt = e2e_step(i, nxt, i + 1 == NB)
+            warm.append(cur)
         torch.cuda.synchronize(dev)
-        ta.tree_attn_check(keep, comp_s)
+        ta.tree_attn_check(warm[-1], comp_s)
+        del warm
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(comp_s)
         h2d_s.wait_event(e0)
         d2h_s.wait_event(e0)
-        plans = []
+        plans, nxt = [], None
         for i in range(e2e_steps):
-            plans.append(e2e_step(i))
+            cur, nxt = e2e_step(i, nxt, i + 1 == e2e_steps)
+            plans.append(cur)
             if len(plans) > NB:
                 plans.pop(0)                                  # freed in comp_s order, after its use
         comp_s.wait_stream(d2h_s)
@@ -661,7 +671,7 @@ def main():
         e1.record(comp_s)
         torch.cuda.synchronize(dev)
         ta.tree_attn_check(plans[-1], comp_s)
-        del keep, plans
+        del plans
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
         e2e = {"value": (flops_fwd + flops_bwd) * world / e2e_ms / 1e9, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
