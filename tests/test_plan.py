@@ -218,6 +218,12 @@ def test_empty_dag():
     plan = host_plan(ep, page_table=np.zeros(0, np.int32))
     st = ta.tree_attn_plan_stats(plan)
     assert st["n_rows"] == 0 and st["n_blocks"] == 0 and st["pairs"] == 0
+    assert st["n_fwd_items"] == 0 and st["n_fwd_split"] == 0
+    # a forced split cap on an empty DAG: still no work items
+    forced = host_plan(ep, page_table=np.zeros(0, np.int32), fwd_split_tiles=1)
+    stf, exf = ta.tree_attn_plan_stats(forced), ta.tree_attn_plan_export(forced)
+    assert stf["n_fwd_items"] == 0 and stf["n_fwd_split"] == 0
+    assert exf["fwd_items"].shape == (0, 4) and exf["fwd_combine"].shape == (0, 4)
 
 
 def _expect(code, ep, **kw):
