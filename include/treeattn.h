@@ -174,7 +174,8 @@ typedef struct {
  *   entries[4*n_entries]               query-major {key tile, lo, hi, flags}
  *   t_entries[4*n_entries]             key-tile-major {block, lo, hi, flags}
  *   chunks[4*n_chunks]                 {key tile, first t_entry, end t_entry, partial slot or -1}
- *   fwd_order[n_blocks]                order in which query blocks are launched
+ *   fwd_order[n_blocks]                query blocks, longest first: the dQ kernel's launch
+ *                                      order (the forward's items follow it, see fwd_items)
  *   fblk_ptr[n_blocks+1], ftiles[8*n_ftiles]
  *                                      per block: the packed key tiles the forward and dQ
  *                                      kernels visit -- 4 slots of 32 key rows each:
