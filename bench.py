@@ -517,8 +517,13 @@ def main():
         ta.tree_attn_fwd(plan, q, k_pool, v_pool, o, lse)
         ta.tree_attn_bwd(plan, q, k_pool, v_pool, o, lse, d_o, dq, dk_pool, dv_pool, ws)
 
-    for _ in range(args.warmup):
+    cold = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for w in range(args.warmup):
+        if w == 0:
+            cold[0].record(stream)
         step()
+        if w == 0:
+            cold[1].record(stream)
     ta.tree_attn_check(plan)
 
     # ---------------------------------------------------------------- timed region
@@ -557,6 +562,11 @@ def main():
     n_reduce = st["n_partial_slots"] > 0
     n_fwd_split = st["n_fwd_split"] > 0
     kern_ms = {"fwd": avg(0, 1), "delta": avg(2, 3), "dq": avg(3, 4), "dkdv": avg(4, 5), "reduce": avg(5, 6)}
+    # per-step times (first kernel's start to last kernel's end) and the first warm-up step,
+    # the one that ran with cold caches and TLBs
+    step_times = sorted(trace[k][0].elapsed_time(trace[k][6]) for k in range(K))
+    step_ms = {"median": round(statistics.median(step_times), 4), "min": round(step_times[0], 4),
+               "max": round(step_times[-1], 4), "cold": round(cold[0].elapsed_time(cold[1]), 4) if args.warmup else None}
     flops_fwd, flops_bwd = st["fwd_flops"], st["bwd_flops"]
     base = ep.head_dim * ep.num_q_heads * st["pairs"]
     algo = {"fwd": 4 * base, "dq": 6 * base, "dkdv": 8 * base}
@@ -690,6 +700,7 @@ def main():
         "fwdbwd_frac_of_nominal": value / world / NOMINAL_BF16_TFLOPS,
         "peak_tflops": {"burst": burst, "sustained": sustained, "kind": peak_kind},
         "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()},
+        "step_ms": step_ms,
         "plan_ms": statistics.median(plan_times),
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": sustained,
                      "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": traffic,
